@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-pool attention hot path on GB300.
+
+A step is one decode step of the Qwen3-0.6B-shaped workload (28 layers,
+batch 64, H_q 16, H_kv 8, head_dim 128, page_size 1, contexts U[512,4096]):
+per layer, store_kv of the 64 new tokens, then split-KV decode attention
+(partial kernel + LSE merge kernel).  The metric is paged decode-attention
+HBM GB/s (algorithmic bytes / time) with tokens/s beside it; the extend
+(chunked-prefill) kernel is measured on the radix-shared extend workload in
+TFLOP/s as a second object.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+
+Under torchrun (N > 1) each rank runs its own copy of the workload (data
+parallel over requests, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+
+
+# --------------------------------------------------------------------------- #
+# algorithmic work
+# --------------------------------------------------------------------------- #
+def decode_layer_bytes(case) -> int:
+    """Bytes one decode-attention call must move at minimum: each context
+    token's K and V row for every KV head, its page-table entry, the queries,
+    the outputs and seq_lens (real requests; padding requests read one row)."""
+    Hkv, d, Hq = case.num_kv_heads, case.head_dim, case.num_q_heads
+    ctx = int(case.seq_lens[:case.num_real].sum())
+    dummy = int(case.batch - case.num_real) > 0
+    kv_rows = ctx + (1 if dummy else 0)
+    return (kv_rows * 2 * Hkv * d * 2 + ctx * 4 + case.batch * Hq * d * 2 * 2 + case.batch * 4)
+
+
+def store_layer_bytes(case) -> int:
+    """store_kv: read k and v rows, write them into the pool, read out_loc."""
+    return case.batch * (2 * 2 * case.num_kv_heads * case.head_dim * 2 + 4)
+
+
+def extend_flops(case) -> float:
+    """Causal-visible FLOPs: 4 d H_q (E C + E(E+1)/2) per request chunk."""
+    f = 0.0
+    d, Hq = case.head_dim, case.num_q_heads
+    for b in case.batches:
+        for C, E in zip(b.cached_lens.tolist(), b.extend_lens.tolist()):
+            f += 4.0 * d * Hq * (E * C + E * (E + 1) / 2)
+    return f
+
+
+# --------------------------------------------------------------------------- #
+# peaks, clocks, ncu traffic
+# --------------------------------------------------------------------------- #
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = None
+        self.ident = ident
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.ident:
+                cmd += ["-i", self.ident]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def profile_traffic(kernel_file: str, summary_name: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    summary is missing or was taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    src = os.path.join(ROOT, "paged_kv_cache_row_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != digest:
+        return None
+    return float(m.group(1))
+
+
+# --------------------------------------------------------------------------- #
+# distributed plumbing
+# --------------------------------------------------------------------------- #
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- #
+# the oracle on the host cores (CPU baseline and the reference arm)
+# --------------------------------------------------------------------------- #
+def oracle_decode_sample(case, pool_t, k_new, v_new, q, layers, reqs):
+    """Prepare host inputs for oracle decode of `reqs` on `layers` (store_kv of
+    their new rows, then decode).  Returns (callable, algorithmic bytes)."""
+    import numpy as np
+    import oracle
+    orc = oracle.get()
+    W = case.page_table.shape[1]
+    rows = torch.cat([case.page_table[r, :int(case.seq_lens[r])] for r in reqs]).long()
+    uniq = torch.unique(rows)
+    idx = uniq.to(pool_t.device)
+
+    def u16(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+    pos = {int(x): i for i, x in enumerate(uniq.tolist())}
+    pt = torch.zeros((len(reqs), W), dtype=torch.int32)
+    sl = torch.zeros(len(reqs), dtype=torch.int32)
+    for i, r in enumerate(reqs):
+        n = int(case.seq_lens[r])
+        sl[i] = n
+        pt[i, :n] = torch.tensor([pos[int(x)] for x in case.page_table[r, :n].tolist()],
+                                 dtype=torch.int32)
+    loc = torch.tensor([pos[int(case.out_loc[r])] for r in reqs], dtype=torch.int32)
+    per_layer = []
+    for l in layers:
+        hk, hv = u16(pool_t[0, l].index_select(0, idx)), u16(pool_t[1, l].index_select(0, idx))
+        per_layer.append((hk, hv, k_new[l][reqs].cpu(), v_new[l][reqs].cpu(), q[l][reqs].cpu()))
+    Hkv, d, Hq = case.num_kv_heads, case.head_dim, case.num_q_heads
+    ctx = int(sl.sum())
+    nbytes = len(layers) * (ctx * (2 * Hkv * d * 2 + 4) + len(reqs) * (Hq * d * 4 + 4)
+                            + len(reqs) * (2 * 2 * Hkv * d * 2 + 4))
+
+    def run():
+        for hk, hv, kn, vn, qq in per_layer:
+            k2, v2 = hk.copy(), hv.copy()
+            orc.store_kv(k2, v2, kn, vn, loc)
+            orc.decode(qq, k2, v2, pt, sl, case.sm_scale)
+
+    return run, nbytes
+
+
+def cpu_cores_used() -> int:
+    return 1  # the oracle is single-threaded C
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm
+# --------------------------------------------------------------------------- #
+def run_gpu(args, world, rank, local):
+    import paged_kv_cache_row_gb300 as mk
+    from paged_kv_cache_row_gb300 import build as mkbuild
+    if rank == 0:
+        mkbuild.build()
+    barrier(world)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = measured_peaks()
+
+    case = workloads.decode_qwen3_0p6b(num_layers=args.layers)
+    L, B, Hq, Hkv, d = case.num_layers, case.batch, case.num_q_heads, case.num_kv_heads, case.head_dim
+    pool_t, k_new, v_new, q = workloads.make_decode_values(case, dev)
+    pool = mk.KVPool(pool_t, case.page_size)
+    pt, sl, loc = case.page_table.to(dev), case.seq_lens.to(dev), case.out_loc.to(dev)
+    ws = mk.decode_workspace(B, Hq, pool)
+    outs = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(kk=k_new, vv=v_new, qq=q, ptab=pt, seq=sl, oloc=loc):
+        for l in range(L):
+            mk.minisgl_store_kv(pool, l, kk[l], vv[l], oloc)
+            mk.minisgl_decode_attn(pool, l, qq[l], ptab, seq, case.sm_scale, out=outs[l],
+                                   workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps ----
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms_local, world)
+
+    dec_b = decode_layer_bytes(case)
+    st_b = store_layer_bytes(case)
+    step_bytes = L * (dec_b + st_b)
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    tokens_s = world * case.num_real / (ms * 1e-3)
+
+    # ---- per-call durations of the dominant call, CUDA events on the launch stream ----
+    n_rep = max(3, min(args.steps, 50))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(n_rep * L)]
+    i = 0
+    for _ in range(n_rep):
+        for l in range(L):
+            a, b_, c = ev[i]
+            a.record(stream)
+            mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
+            b_.record(stream)
+            mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, out=outs[l], workspace=ws)
+            c.record(stream)
+            i += 1
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(b_.elapsed_time(c) for _, b_, c in ev)
+    st_ms = statistics.mean(a.elapsed_time(b_) for a, b_, _ in ev)
+    achieved = dec_b / (dec_ms * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    traffic = profile_traffic("decode.cu", "decode_qwen3_0p6b.md")
+
+    # ---- e2e: the same step through the C ABI with host buffers ----
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = [pin(k_new), pin(v_new), pin(q), pin(case.page_table), pin(case.seq_lens), pin(case.out_loc)]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    h_out = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for h, dd in zip(h_in, d_in):
+            dd.copy_(h, non_blocking=True)
+        step(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5])
+        h_out.copy_(outs, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 4)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world)
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    # ---- extend: radix-shared chunked prefill, store_kv + extend per batch ----
+    ext = None
+    if not args.no_extend:
+        ecase = workloads.extend_radix_shared()
+        epool_t, per_batch = workloads.make_extend_values(ecase, dev)
+        epool = mk.KVPool(epool_t)
+        eargs = [(b.page_table.to(dev), b.cached_lens.to(dev), b.extend_lens.to(dev),
+                  b.q_offsets.to(dev), b.out_loc.to(dev)) for b in ecase.batches]
+        eouts = [torch.empty_like(qq) for _, _, qq in per_batch]
+
+        def estep():
+            for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
+                mk.minisgl_store_kv(epool, 0, k, v, eloc)
+                mk.minisgl_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, ecase.sm_scale, out=eo)
+
+        for _ in range(args.warmup):
+            estep()
+        torch.cuda.synchronize()
+        eks = max(5, args.steps // 10)
+        xev = []
+        for _ in range(eks):
+            for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
+                mk.minisgl_store_kv(epool, 0, k, v, eloc)
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                mk.minisgl_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, ecase.sm_scale, out=eo)
+                b_.record(stream)
+                xev.append((a, b_))
+        torch.cuda.synchronize()
+        ext_ms_per_pass = sum(a.elapsed_time(b_) for a, b_ in xev) / eks
+        fl = extend_flops(ecase)
+        tf = fl / (ext_ms_per_pass * 1e-3) / 1e12
+        launch_fl = fl / len(ecase.batches)
+        launch_ms = ext_ms_per_pass / len(ecase.batches)
+        ext = {
+            "workload": ecase.name, "metric": "extend-attn TFLOP/s (causal-visible FLOPs)",
+            "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_pass": round(ext_ms_per_pass, 4),
+            "batches": len(ecase.batches), "tokens": int(sum(ecase.extend_lens)),
+            "roofline": {"bound": "tensor", "achieved": round(launch_fl / (launch_ms * 1e-3) / 1e12, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(launch_fl / (launch_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                         "traffic": profile_traffic("extend.cu", "extend_radix_shared.md"),
+                         "peak_source": peaks["source"] + " bf16 dense burst"},
+        }
+        del epool_t, per_batch
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        reqs = list(range(0, B, 8))
+        run, nbytes = oracle_decode_sample(case, pool_t, k_new, v_new, q, [0], reqs)
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            run()
+            n += 1
+            if time.perf_counter() - t0 > 10.0 or n >= 200:
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
+               "kind": "oracle",
+               "sample": f"store_kv + decode of requests {reqs} (of {B}) on layer 0, "
+                         f"repeated {n}x, {dt:.1f} s, single-threaded fp64 C"}
+
+    gpu_launches = args.steps * L * 3
+    line = {
+        "metric": "paged decode-attn HBM GB/s (algorithmic bytes, store_kv + decode per layer)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(tokens_s, 1),
+        "config": {"workload": case.name, "layers": L, "batch": B, "H_q": Hq, "H_kv": Hkv,
+                   "head_dim": d, "page_size": case.page_size,
+                   "context_tokens": int(case.seq_lens.sum()),
+                   "l2": "inputs larger than L2: each layer reads %.0f MB of K/V, a step %.1f GB"
+                         % (dec_b / 1e6, step_bytes / 1e9),
+                   "parallelism": f"dp{world} (independent batches per GPU)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_attn call (split-KV partial + LSE merge kernels)",
+                     "algorithmic_bytes_per_launch": dec_b, "ms_per_launch": round(dec_ms, 5),
+                     "peak_source": peaks["source"] + " hbm copy"},
+        "store_kv": {"ms_per_launch": round(st_ms, 5),
+                     "achieved_gbs": round(st_b / (st_ms * 1e-3) / 1e9, 1)},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": gpu_launches,
+        "extend": ext,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# reference arm: the oracle on the host cores
+# --------------------------------------------------------------------------- #
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    case = workloads.decode_qwen3_0p6b()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    pool_t, k_new, v_new, q = workloads.make_decode_values(case, dev)
+    reqs = [0, 21, 42]
+    run, nbytes = oracle_decode_sample(case, pool_t, k_new, v_new, q, [0], reqs)
+    del pool_t
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    sample = (f"each step: store_kv + decode of requests {reqs} of the {case.name} batch on "
+              f"layer 0 ({nbytes / 1e6:.1f} MB algorithmic), single-threaded fp64 C oracle")
+    line = {
+        "impl": "reference",
+        "metric": "paged decode-attn HBM GB/s (algorithmic bytes, store_kv + decode per layer)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case.name, "layers": case.num_layers, "batch": case.batch,
+                   "sample_requests": reqs, "parallelism": "single CPU thread"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--layers", type=int, default=28,
+                    help="layers of the decode workload (28 = the full model; fewer only for "
+                         "profiler captures that must stay small)")
+    ap.add_argument("--no-extend", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * minisgl.h -- C ABI of the GB300 (sm_103a) paged KV-pool attention library.
+ *
+ * Three operations make up the attention step of a serving engine that keeps
+ * its KV cache in one paged pool (the mini-sglang design):
+ *
+ *   minisgl_store_kv     scatter this step's new K/V token rows into the pool
+ *   minisgl_decode_attn  one query token per request, split-KV, then an LSE merge
+ *   minisgl_extend_attn  causal attention for the new tokens of chunked prefill
+ *
+ * Sources of the definitions (page title, section):
+ *   [deep-dive]  "mini-sglang 架构深度解读" (mini-sglang architecture deep dive,
+ *                tinymind.me): section 6.2 MHAKVCache layout, section 3
+ *                page-table figure, section 5 attention backends.
+ *   [learn]      "doc-mini-sglang-learn" (mini-sglang learning notes): the
+ *                paged KV pool chapter (pool shape, store_kv, dummy page,
+ *                page_table alignment, page_size), the request-state passage
+ *                (cached_len / extend_len), the chunked-prefill chapter and
+ *                the attention-backend chapter (FlashDecoding-style split-KV).
+ *   [sglang]     "SGLang 源码导读" (SGLang source reading guide): ForwardBatch
+ *                fields seq_lens, extend_prefix_lens, extend_seq_lens,
+ *                out_cache_loc.
+ *
+ * Conventions for every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or keeps device memory, and keeps no
+ *     state between calls besides a thread-local error string.
+ *   - Element type is bf16 for K, V, Q and the output (MINISGL_BF16); index
+ *     tensors are int32.  Strides are in elements.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  No call synchronises with the host, so every call can be
+ *     captured in a CUDA graph as long as its pointers stay fixed.
+ *   - Return value: MINISGL_OK, or a negative MINISGL_ERR_* code with a
+ *     message available from minisgl_last_error().  Argument checks happen on
+ *     the host before any launch; a launch failure returns MINISGL_ERR_CUDA.
+ *   - Kernels never trap.  Index VALUES live on the device and are not checked
+ *     by the host: a page_table / out_loc entry outside [0, num_rows) is a
+ *     caller error; the kernels clamp it into the pool so that no access
+ *     leaves the caller's buffers, and the affected results are unspecified.
+ *     seq_lens / cached_lens + extend_lens larger than the page_table width
+ *     are likewise clamped to the width.
+ *   - Alignment: pool bases, k/v/q/out bases and all row strides must give
+ *     16-byte aligned rows (bases 16-byte aligned, strides multiples of 8
+ *     elements).
+ */
+#ifndef MINISGL_H
+#define MINISGL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MINISGL_OK = 0,
+    MINISGL_ERR_ARG = -1,         /* null pointer, negative size, bad layer */
+    MINISGL_ERR_DTYPE = -2,       /* pool dtype is not MINISGL_BF16 */
+    MINISGL_ERR_SHAPE = -3,       /* head counts / strides / alignment inconsistent */
+    MINISGL_ERR_UNSUPPORTED = -4, /* head_dim or group size this build has no kernel for */
+    MINISGL_ERR_CUDA = -5,        /* a CUDA call or kernel launch failed */
+    MINISGL_ERR_WORKSPACE = -6    /* workspace missing or too small */
+};
+
+enum { MINISGL_BF16 = 1 };
+
+/*
+ * The KV pool [deep-dive 6.2; learn, paged KV pool]: logically
+ * (2, L, R, H_kv, d) -- K/V, layer, physical token row, KV head, head dim.
+ * Per layer, K and V are each an (R, H_kv, d) array of token rows and a
+ * token's physical position is its row number.  page_size s only describes
+ * how rows were allocated (R = P * s); the kernels never assume pages are
+ * contiguous, because page_table entries are raw rows.
+ *   element (kv, l, row, h, c) of K is at  k_base + l*layer_stride + row*row_stride + h*head_dim + c
+ * LayerFirst allocation gives layer_stride = R*H_kv*d and row_stride = H_kv*d;
+ * PageFirst (pages outermost) gives layer_stride = H_kv*d and
+ * row_stride = L*H_kv*d.  Both are accepted.
+ */
+typedef struct {
+    void *k_base;          /* device: K of layer 0, row 0 */
+    void *v_base;          /* device: V of layer 0, row 0 */
+    int64_t layer_stride;  /* elements between layers */
+    int64_t row_stride;    /* elements between physical rows; >= num_kv_heads*head_dim */
+    int32_t num_layers;
+    int32_t num_rows;      /* R, including any dummy page rows */
+    int32_t num_kv_heads;  /* H_kv local to this GPU */
+    int32_t head_dim;      /* d: 64 or 128 */
+    int32_t page_size;     /* s: informational (1, 16, 32, 64 ...) */
+    int32_t dtype;         /* MINISGL_BF16 */
+} minisgl_kv_pool;
+
+/*
+ * store_kv [learn, paged KV pool: "store_kv" passage; deep-dive 6.2].
+ * For i < n_tokens and every KV head h and channel c:
+ *     K[layer][out_loc[i]][h][c] = k[i*k_tok_stride + h*head_dim + c]
+ *     V[layer][out_loc[i]][h][c] = v[i*v_tok_stride + h*head_dim + c]
+ * k, v: device bf16, one row of num_kv_heads*head_dim elements per token.
+ * out_loc: device int32 [n_tokens], physical rows.  Bit-exact copy.  Tokens
+ * that share a row (CUDA-Graph padding requests all write the dummy row)
+ * race; the row ends up holding one of their values, so callers give such
+ * tokens identical k/v.  n_tokens == 0 is a no-op.
+ */
+int minisgl_store_kv(const minisgl_kv_pool *pool, int32_t layer, const void *k, const void *v,
+                     int64_t k_tok_stride, int64_t v_tok_stride, const int32_t *out_loc,
+                     int32_t n_tokens, void *stream);
+
+/*
+ * Workspace size for minisgl_decode_attn, in bytes, for up to `max_splits`
+ * partial results per (request, KV head) (2 <= max_splits <= 256; 16 is a
+ * good default).  Layout of a workspace of this size, for the record (the
+ * caller does not need to read it):
+ *   int32 split_count[batch * num_kv_heads]            (at offset 0, padded to 256 B)
+ *   float lse[batch * num_q_heads * max_splits]        natural-log LSE per partial
+ *   float o[batch * num_q_heads * max_splits * head_dim] normalised partial outputs
+ * Index of partial s of request r, query head h: (r*num_q_heads + h)*max_splits + s.
+ */
+size_t minisgl_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_splits);
+
+/*
+ * Decode attention [learn, paged KV pool and attention-backend chapters;
+ * deep-dive 5.3 PagedAttention].  For request r < batch, query head
+ * h < num_q_heads, KV head g = h / (num_q_heads / num_kv_heads) (GQA, contiguous
+ * groups), and n = seq_lens[r] (the context INCLUDING the token stored this
+ * step by minisgl_store_kv):
+ *     S_j = sm_scale * <q[r,h,:], K[layer][page_table[r*pt_row_stride + j]][g][:]>,  j < n
+ *     out[r,h,:] = sum_j softmax(S)_j * V[layer][page_table[r*pt_row_stride + j]][g][:]
+ * q: device bf16 [batch, num_q_heads, head_dim] contiguous.
+ * page_table: device int32, row r at page_table + r*pt_row_stride, raw
+ *   physical rows; columns j >= seq_lens[r] are never read.
+ * seq_lens: device int32 [batch].  n == 0 gives out = 0.
+ * out: device bf16 [batch, num_q_heads, head_dim] contiguous.
+ * workspace: device, caller-owned, at least
+ *   minisgl_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, 2)
+ *   bytes; the number of splits the kernel may use grows with its size.
+ * split_tokens: 0 lets the kernel balance the KV length over all SMs (the
+ *   normal setting); a positive value asks for about that many tokens per
+ *   partial result (rounded up to 16, and raised if the workspace is too
+ *   small for it) -- used to test the merge at chosen split counts.
+ * Launches a split-KV partial kernel and, when any request was split, the
+ * log-sum-exp merge kernel, both on `stream`.
+ * Supported: head_dim in {64, 128}; 1 <= num_q_heads/num_kv_heads <= 16;
+ * batch <= 4096.
+ */
+int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                        int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                        int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
+                        float sm_scale, void *out, void *workspace, size_t workspace_bytes,
+                        int32_t split_tokens, void *stream);
+
+/*
+ * Extend (chunked-prefill) attention [learn: request-state passage
+ * extend_len = device_len - cached_len, chunked-prefill chapter; sglang:
+ * ForwardBatch extend_prefix_lens / extend_seq_lens].  Request r has
+ * C = cached_lens[r] tokens already in the pool and E = extend_lens[r] new
+ * tokens, whose K/V the caller has already stored (minisgl_store_kv) at the
+ * rows page_table[r, C .. C+E-1].  New token t (0 <= t < E) is at absolute
+ * position C + t and attends causally to logical tokens 0 .. C + t:
+ *     out[q_offsets[r]+t, h, :] = sum_{j <= C+t} softmax_j(sm_scale * <q[q_offsets[r]+t,h,:], K_j[g]>) V_j[g]
+ * q: device bf16 [total_q_tokens, num_q_heads, head_dim] packed in request order.
+ * q_offsets: device int32 [batch+1], exclusive prefix sum of extend_lens
+ *   (q_offsets[batch] == total_q_tokens).
+ * cached_lens, extend_lens: device int32 [batch].
+ * page_table: as for decode; pt_width columns per row.
+ * out: device bf16 [total_q_tokens, num_q_heads, head_dim].
+ * Runs on the tensor cores (tcgen05, accumulators in tensor memory).
+ * Supported: head_dim 128; num_q_heads/num_kv_heads in {1, 2, 4, 8, 16};
+ * batch <= 4096.
+ */
+int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                        int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                        int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
+                        const int32_t *extend_lens, const int32_t *q_offsets,
+                        int32_t total_q_tokens, float sm_scale, void *out, void *stream);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char *minisgl_last_error(void);
+
+/* Number of streaming multiprocessors of the current device (0 on error);
+ * the persistent kernels size their grids from it. */
+int32_t minisgl_device_sm_count(void);
+
+/* Debugging aid: how many bounded waits inside the tensor-core kernels ran
+ * out of time since the library was loaded on the current device.  A
+ * non-zero count means some minisgl_extend_attn output is garbage.  This call
+ * synchronises with the device (it reads a device counter), so it is not
+ * for the hot path. */
+int minisgl_debug_timeout_count(uint32_t *count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MINISGL_H */

@@ -1,0 +1,246 @@
+"""Paged KV-pool attention for GB300 (sm_103a): Python binding of libminisgl.so.
+
+The C library (include/minisgl.h) does all the work in hand-written CUDA
+kernels; this module only marshals torch tensors into pointers, sizes and the
+current CUDA stream.  There is no fallback: if the library is not built, or a
+call fails, an exception is raised.
+
+Entry points (same names as the C ABI):
+    minisgl_store_kv(pool, layer, k, v, out_loc)
+    minisgl_decode_attn(pool, layer, q, page_table, seq_lens, sm_scale, ...)
+    minisgl_extend_attn(pool, layer, q, page_table, cached_lens, extend_lens, q_offsets, sm_scale, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "KVPool", "minisgl_store_kv", "minisgl_decode_attn", "minisgl_extend_attn",
+    "minisgl_decode_workspace_bytes", "minisgl_device_sm_count", "minisgl_debug_timeout_count",
+    "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = [
+    "minisgl_store_kv", "minisgl_decode_workspace_bytes", "minisgl_decode_attn",
+    "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
+    "minisgl_debug_timeout_count",
+]
+
+MINISGL_BF16 = 1
+
+
+class MinisglError(RuntimeError):
+    pass
+
+
+class _PoolDesc(ctypes.Structure):
+    _fields_ = [
+        ("k_base", ctypes.c_void_p), ("v_base", ctypes.c_void_p),
+        ("layer_stride", ctypes.c_int64), ("row_stride", ctypes.c_int64),
+        ("num_layers", ctypes.c_int32), ("num_rows", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libminisgl.so (built by paged_kv_cache_row_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m paged_kv_cache_row_gb300.build`"
+                          " (or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    P = ctypes.POINTER(_PoolDesc)
+    lib.minisgl_store_kv.argtypes = [P, i32, vp, vp, i64, i64, vp, i32, vp]
+    lib.minisgl_store_kv.restype = ctypes.c_int
+    lib.minisgl_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.minisgl_decode_workspace_bytes.restype = sz
+    lib.minisgl_decode_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, f32, vp, vp, sz, i32, vp]
+    lib.minisgl_decode_attn.restype = ctypes.c_int
+    lib.minisgl_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, f32, vp, vp]
+    lib.minisgl_extend_attn.restype = ctypes.c_int
+    lib.minisgl_last_error.argtypes = []
+    lib.minisgl_last_error.restype = ctypes.c_char_p
+    lib.minisgl_device_sm_count.argtypes = []
+    lib.minisgl_device_sm_count.restype = i32
+    lib.minisgl_debug_timeout_count.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.minisgl_debug_timeout_count.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        msg = load_library().minisgl_last_error().decode(errors="replace")
+        raise MinisglError(f"{what} failed ({rc}): {msg}")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not t.is_cuda:
+        raise MinisglError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MinisglError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+class KVPool:
+    """A paged KV pool: one bf16 tensor of logical shape (2, L, R, H_kv, d).
+
+    `tensor` may be LayerFirst (contiguous (2, L, R, H_kv, d)) or a permuted
+    PageFirst view; only strides are read.  The pool is caller-owned device
+    memory; the library keeps no reference to it."""
+
+    def __init__(self, tensor: torch.Tensor, page_size: int = 1):
+        if tensor.dim() != 5 or tensor.shape[0] != 2:
+            raise MinisglError("pool tensor must have shape (2, L, R, H_kv, d)")
+        _need(tensor, "pool", torch.bfloat16)
+        if tensor.stride(4) != 1 or tensor.stride(3) != tensor.shape[4]:
+            raise MinisglError("pool rows must be (H_kv, d) contiguous")
+        self.tensor = tensor
+        self.page_size = page_size
+        _, L, R, H, d = tensor.shape
+        self.num_layers, self.num_rows, self.num_kv_heads, self.head_dim = L, R, H, d
+        self.desc = _PoolDesc(
+            k_base=tensor[0].data_ptr(), v_base=tensor[1].data_ptr(),
+            layer_stride=tensor.stride(1), row_stride=tensor.stride(2),
+            num_layers=L, num_rows=R, num_kv_heads=H, head_dim=d, page_size=page_size,
+            dtype=MINISGL_BF16)
+
+    def k(self, layer: int) -> torch.Tensor:
+        return self.tensor[0, layer]
+
+    def v(self, layer: int) -> torch.Tensor:
+        return self.tensor[1, layer]
+
+
+def kv_pool_bytes(num_layers: int, num_kv_heads: int, head_dim: int, num_tokens: int,
+                  elem_bytes: int = 2) -> int:
+    """Bytes the pool needs to hold num_tokens token rows in every layer, K and V."""
+    return 2 * num_layers * num_kv_heads * head_dim * num_tokens * elem_bytes
+
+
+def minisgl_store_kv(pool: KVPool, layer: int, k: torch.Tensor, v: torch.Tensor,
+                     out_loc: torch.Tensor, stream=None) -> None:
+    """pool[K|V][layer][out_loc[i]] = k[i] | v[i] for every new token i (bit-exact)."""
+    lib = load_library()
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16)
+    _need(out_loc, "out_loc", torch.int32)
+    n = out_loc.numel()
+    row = pool.num_kv_heads * pool.head_dim
+    for t, nm in ((k, "k"), (v, "v")):
+        if t.shape[0] != n or t[0].numel() != row or not t[0].is_contiguous():
+            raise MinisglError(f"{nm} must be [n_tokens, H_kv, d] with contiguous rows")
+    if not out_loc.is_contiguous():
+        raise MinisglError("out_loc must be contiguous")
+    _check(lib.minisgl_store_kv(ctypes.byref(pool.desc), layer, _ptr(k), _ptr(v), k.stride(0),
+                                v.stride(0), _ptr(out_loc), n, _stream(stream)), "store_kv")
+
+
+def minisgl_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                   max_splits: int = 16) -> int:
+    return int(load_library().minisgl_decode_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                             head_dim, max_splits))
+
+
+_ws_cache = {}
+
+
+def decode_workspace(batch: int, num_q_heads: int, pool: KVPool, max_splits: int = 16,
+                     device=None) -> torch.Tensor:
+    """A workspace tensor for minisgl_decode_attn, cached per shape and device."""
+    device = torch.device(device or pool.tensor.device)
+    nbytes = minisgl_decode_workspace_bytes(batch, num_q_heads, pool.num_kv_heads, pool.head_dim,
+                                            max_splits)
+    key = (device, nbytes)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def minisgl_decode_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: torch.Tensor,
+                        seq_lens: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, split_tokens: int = 0,
+                        max_splits: int = 16, stream=None) -> torch.Tensor:
+    """Decode attention of q [B, H_q, d] over each request's page_table row."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16)
+    _need(page_table, "page_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, Hq, d = q.shape
+    if not q.is_contiguous() or d != pool.head_dim:
+        raise MinisglError("q must be contiguous [B, H_q, head_dim]")
+    if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if seq_lens.numel() != B or not seq_lens.is_contiguous():
+        raise MinisglError("seq_lens must be contiguous [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, pool, max_splits)
+    _check(lib.minisgl_decode_attn(ctypes.byref(pool.desc), layer, _ptr(q), Hq, _ptr(page_table), B,
+                                   page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
+                                   float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                   split_tokens, _stream(stream)), "decode_attn")
+    return out
+
+
+def minisgl_extend_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: torch.Tensor,
+                        cached_lens: torch.Tensor, extend_lens: torch.Tensor,
+                        q_offsets: torch.Tensor, sm_scale: float,
+                        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal extend attention of the packed new tokens q [T, H_q, d]."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16)
+    for t, nm in ((page_table, "page_table"), (cached_lens, "cached_lens"),
+                  (extend_lens, "extend_lens"), (q_offsets, "q_offsets")):
+        _need(t, nm, torch.int32)
+    T, Hq, d = q.shape
+    B = cached_lens.numel()
+    if not q.is_contiguous() or d != pool.head_dim:
+        raise MinisglError("q must be contiguous [T, H_q, head_dim]")
+    if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if extend_lens.numel() != B or q_offsets.numel() != B + 1:
+        raise MinisglError("extend_lens must be [B] and q_offsets [B+1]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16)
+    _check(lib.minisgl_extend_attn(ctypes.byref(pool.desc), layer, _ptr(q), Hq, _ptr(page_table), B,
+                                   page_table.stride(0), page_table.shape[1], _ptr(cached_lens),
+                                   _ptr(extend_lens), _ptr(q_offsets), T, float(sm_scale), _ptr(out),
+                                   _stream(stream)), "extend_attn")
+    return out
+
+
+def minisgl_device_sm_count() -> int:
+    return int(load_library().minisgl_device_sm_count())
+
+
+def minisgl_debug_timeout_count() -> int:
+    c = ctypes.c_uint32(0)
+    _check(load_library().minisgl_debug_timeout_count(ctypes.byref(c)), "debug_timeout_count")
+    return int(c.value)

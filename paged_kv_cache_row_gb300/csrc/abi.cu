@@ -1,0 +1,243 @@
+// abi.cu -- the extern "C" entry points declared in include/minisgl.h.
+//
+// Host-side argument checks, the thread-local error string, workspace
+// carving, and the launches.  No entry point allocates device memory or
+// synchronises with the device.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "kernels.h"
+#include "minisgl.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_pool(const minisgl_kv_pool *p, int32_t layer, const char *who) {
+    if (!p) return fail(MINISGL_ERR_ARG, "%s: pool descriptor is NULL", who);
+    if (p->dtype != MINISGL_BF16) return fail(MINISGL_ERR_DTYPE, "%s: pool dtype must be bf16", who);
+    if (!p->k_base || !p->v_base) return fail(MINISGL_ERR_ARG, "%s: pool base is NULL", who);
+    if (p->head_dim != 64 && p->head_dim != 128)
+        return fail(MINISGL_ERR_UNSUPPORTED, "%s: head_dim %d not in {64, 128}", who, p->head_dim);
+    if (p->num_kv_heads < 1 || p->num_rows < 1 || p->num_layers < 1)
+        return fail(MINISGL_ERR_SHAPE, "%s: pool sizes must be positive", who);
+    if (p->row_stride < (int64_t)p->num_kv_heads * p->head_dim || p->row_stride % 8 != 0)
+        return fail(MINISGL_ERR_SHAPE, "%s: row_stride %lld must be >= H_kv*d and a multiple of 8",
+                    who, (long long)p->row_stride);
+    if (p->layer_stride % 8 != 0 || p->layer_stride < 0)
+        return fail(MINISGL_ERR_SHAPE, "%s: layer_stride must be a non-negative multiple of 8", who);
+    if (!aligned16(p->k_base) || !aligned16(p->v_base))
+        return fail(MINISGL_ERR_SHAPE, "%s: pool bases must be 16-byte aligned", who);
+    if (layer < 0 || layer >= p->num_layers)
+        return fail(MINISGL_ERR_ARG, "%s: layer %d outside [0, %d)", who, layer, p->num_layers);
+    return MINISGL_OK;
+}
+
+const void *layer_ptr(const void *base, const minisgl_kv_pool *p, int32_t layer) {
+    return static_cast<const char *>(base) + (size_t)layer * p->layer_stride * 2;
+}
+
+int cuda_status(cudaError_t e, const char *who) {
+    if (e == cudaSuccess) return MINISGL_OK;
+    return fail(MINISGL_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t ws_bytes(int64_t batch, int64_t hq, int64_t hkv, int64_t d, int64_t splits) {
+    return align256(batch * hkv * 4) + align256(batch * hq * splits * 4) + batch * hq * splits * d * 4;
+}
+
+int check_heads(int32_t hq, int32_t hkv, int max_group, const char *who) {
+    if (hq < 1 || hq % hkv != 0)
+        return fail(MINISGL_ERR_SHAPE, "%s: num_q_heads %d is not a multiple of num_kv_heads %d",
+                    who, hq, hkv);
+    if (hq / hkv > max_group)
+        return fail(MINISGL_ERR_UNSUPPORTED, "%s: group size %d > %d", who, hq / hkv, max_group);
+    return MINISGL_OK;
+}
+
+}  // namespace
+
+namespace minisgl {
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+}  // namespace minisgl
+
+extern "C" {
+
+const char *minisgl_last_error(void) { return g_err.c_str(); }
+
+int32_t minisgl_device_sm_count(void) { return minisgl::device_sm_count(); }
+
+int minisgl_debug_timeout_count(uint32_t *count) {
+    g_err.clear();
+    if (!count) return fail(MINISGL_ERR_ARG, "debug_timeout_count: NULL count");
+    unsigned int c = 0;
+    if (int rc = cuda_status(minisgl::read_kernel_timeouts(&c), "debug_timeout_count")) return rc;
+    *count = c;
+    return MINISGL_OK;
+}
+
+int minisgl_store_kv(const minisgl_kv_pool *pool, int32_t layer, const void *k, const void *v,
+                     int64_t k_tok_stride, int64_t v_tok_stride, const int32_t *out_loc,
+                     int32_t n_tokens, void *stream) {
+    g_err.clear();
+    if (int rc = check_pool(pool, layer, "store_kv")) return rc;
+    if (n_tokens < 0) return fail(MINISGL_ERR_ARG, "store_kv: n_tokens < 0");
+    if (n_tokens == 0) return MINISGL_OK;
+    if (!k || !v || !out_loc) return fail(MINISGL_ERR_ARG, "store_kv: NULL k, v or out_loc");
+    const int64_t row = (int64_t)pool->num_kv_heads * pool->head_dim;
+    if (!aligned16(k) || !aligned16(v))
+        return fail(MINISGL_ERR_SHAPE, "store_kv: k and v must be 16-byte aligned");
+    if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+        return fail(MINISGL_ERR_SHAPE, "store_kv: token strides must be >= H_kv*d and multiples of 8");
+    minisgl::StoreArgs a;
+    a.k_layer = const_cast<void *>(layer_ptr(pool->k_base, pool, layer));
+    a.v_layer = const_cast<void *>(layer_ptr(pool->v_base, pool, layer));
+    a.row_stride = pool->row_stride;
+    a.num_rows = pool->num_rows;
+    a.k = k;
+    a.v = v;
+    a.k_tok_stride = k_tok_stride;
+    a.v_tok_stride = v_tok_stride;
+    a.out_loc = out_loc;
+    a.n_tokens = n_tokens;
+    a.row_elems = (int32_t)row;
+    return cuda_status(minisgl::launch_store_kv(a, static_cast<cudaStream_t>(stream)), "store_kv");
+}
+
+size_t minisgl_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_splits) {
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || max_splits < 2 ||
+        max_splits > 256)
+        return 0;
+    return ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_splits);
+}
+
+int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                        int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                        int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
+                        float sm_scale, void *out, void *workspace, size_t workspace_bytes,
+                        int32_t split_tokens, void *stream) {
+    g_err.clear();
+    if (int rc = check_pool(pool, layer, "decode_attn")) return rc;
+    if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "decode_attn")) return rc;
+    if (batch < 0 || batch > 4096) return fail(MINISGL_ERR_ARG, "decode_attn: batch %d outside [0, 4096]", batch);
+    if (batch == 0) return MINISGL_OK;
+    if (!q || !page_table || !seq_lens || !out)
+        return fail(MINISGL_ERR_ARG, "decode_attn: NULL q, page_table, seq_lens or out");
+    if (!aligned16(q) || !aligned16(out))
+        return fail(MINISGL_ERR_SHAPE, "decode_attn: q and out must be 16-byte aligned");
+    if (pt_width < 0 || pt_row_stride < pt_width)
+        return fail(MINISGL_ERR_SHAPE, "decode_attn: need 0 <= pt_width <= pt_row_stride");
+    if (split_tokens < 0) return fail(MINISGL_ERR_ARG, "decode_attn: split_tokens < 0");
+    const int64_t tiles = (int64_t)batch * pool->num_kv_heads * ((pt_width + 15) / 16);
+    if (tiles >= (int64_t(1) << 31))
+        return fail(MINISGL_ERR_UNSUPPORTED, "decode_attn: batch * H_kv * width too large");
+    // the largest split count the workspace holds
+    int splits = 0;
+    if (workspace && ((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)) {
+        for (int s = 256; s >= 2; --s)
+            if (ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, s) <= workspace_bytes) {
+                splits = s;
+                break;
+            }
+    }
+    if (splits < 2)
+        return fail(MINISGL_ERR_WORKSPACE,
+                    "decode_attn: workspace must be 256-byte aligned and hold >= 2 splits (%zu bytes)",
+                    ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, 2));
+    minisgl::DecodeArgs a;
+    a.q = q;
+    a.k_layer = layer_ptr(pool->k_base, pool, layer);
+    a.v_layer = layer_ptr(pool->v_base, pool, layer);
+    a.row_stride = pool->row_stride;
+    a.num_rows = pool->num_rows;
+    a.page_table = page_table;
+    a.pt_stride = pt_row_stride;
+    a.pt_width = pt_width;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.head_dim = pool->head_dim;
+    a.sm_scale = sm_scale;
+    a.out = out;
+    char *ws = static_cast<char *>(workspace);
+    a.split_count = reinterpret_cast<int32_t *>(ws);
+    ws += align256((size_t)batch * pool->num_kv_heads * 4);
+    a.ws_lse = reinterpret_cast<float *>(ws);
+    ws += align256((size_t)batch * num_q_heads * splits * 4);
+    a.ws_o = reinterpret_cast<float *>(ws);
+    a.max_splits = splits;
+    a.split_tokens = split_tokens;
+    return cuda_status(minisgl::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode_attn");
+}
+
+int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                        int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                        int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
+                        const int32_t *extend_lens, const int32_t *q_offsets,
+                        int32_t total_q_tokens, float sm_scale, void *out, void *stream) {
+    g_err.clear();
+    if (int rc = check_pool(pool, layer, "extend_attn")) return rc;
+    if (pool->head_dim != 128)
+        return fail(MINISGL_ERR_UNSUPPORTED, "extend_attn: head_dim %d (only 128)", pool->head_dim);
+    if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "extend_attn")) return rc;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if (G & (G - 1)) return fail(MINISGL_ERR_UNSUPPORTED, "extend_attn: group size %d not a power of 2", G);
+    if (batch < 0 || batch > 4096) return fail(MINISGL_ERR_ARG, "extend_attn: batch %d outside [0, 4096]", batch);
+    if (total_q_tokens < 0) return fail(MINISGL_ERR_ARG, "extend_attn: total_q_tokens < 0");
+    if (batch == 0 || total_q_tokens == 0) return MINISGL_OK;
+    if (!q || !page_table || !cached_lens || !extend_lens || !q_offsets || !out)
+        return fail(MINISGL_ERR_ARG, "extend_attn: NULL pointer argument");
+    if (!aligned16(q) || !aligned16(out))
+        return fail(MINISGL_ERR_SHAPE, "extend_attn: q and out must be 16-byte aligned");
+    if (pt_width < 0 || pt_row_stride < pt_width)
+        return fail(MINISGL_ERR_SHAPE, "extend_attn: need 0 <= pt_width <= pt_row_stride");
+    minisgl::ExtendArgs a;
+    a.q = q;
+    a.k_layer = layer_ptr(pool->k_base, pool, layer);
+    a.v_layer = layer_ptr(pool->v_base, pool, layer);
+    a.row_stride = pool->row_stride;
+    a.num_rows = pool->num_rows;
+    a.page_table = page_table;
+    a.pt_stride = pt_row_stride;
+    a.pt_width = pt_width;
+    a.cached_lens = cached_lens;
+    a.extend_lens = extend_lens;
+    a.q_offsets = q_offsets;
+    a.batch = batch;
+    a.total_q_tokens = total_q_tokens;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.head_dim = pool->head_dim;
+    a.sm_scale = sm_scale;
+    a.out = out;
+    return cuda_status(minisgl::launch_extend(a, static_cast<cudaStream_t>(stream)), "extend_attn");
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// kernels.h -- host-side launch interface between the C ABI (abi.cu) and the
+// kernel translation units.  Internal to the library.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace minisgl {
+
+struct StoreArgs {
+    void *k_layer, *v_layer;      // layer base of K / V in the pool
+    int64_t row_stride;           // elements between pool rows
+    int32_t num_rows;
+    const void *k, *v;            // new rows
+    int64_t k_tok_stride, v_tok_stride;
+    const int32_t *out_loc;
+    int32_t n_tokens;
+    int32_t row_elems;            // num_kv_heads * head_dim
+};
+cudaError_t launch_store_kv(const StoreArgs &a, cudaStream_t s);
+
+struct DecodeArgs {
+    const void *q;                // [B, Hq, D]
+    const void *k_layer, *v_layer;
+    int64_t row_stride;
+    int32_t num_rows;
+    const int32_t *page_table;
+    int64_t pt_stride;
+    int32_t pt_width;
+    const int32_t *seq_lens;
+    int32_t batch, num_q_heads, num_kv_heads, head_dim;
+    float sm_scale;
+    void *out;                    // [B, Hq, D] bf16
+    int32_t *split_count;         // workspace parts
+    float *ws_lse, *ws_o;
+    int32_t max_splits;
+    int32_t split_tokens;         // 0 = automatic
+};
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+
+struct ExtendArgs {
+    const void *q;                // [T, Hq, D]
+    const void *k_layer, *v_layer;
+    int64_t row_stride;
+    int32_t num_rows;
+    const int32_t *page_table;
+    int64_t pt_stride;
+    int32_t pt_width;
+    const int32_t *cached_lens, *extend_lens, *q_offsets;
+    int32_t batch, total_q_tokens, num_q_heads, num_kv_heads, head_dim;
+    float sm_scale;
+    void *out;                    // [T, Hq, D] bf16
+};
+cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s);
+
+int device_sm_count();
+
+// Number of bounded waits that ran out in tensor-core kernels since load
+// (synchronous copy from a device counter).
+cudaError_t read_kernel_timeouts(unsigned int *count);
+
+}  // namespace minisgl

@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every entry point include/minisgl.h declares, and rejects bad
+arguments with the documented error codes before any device work."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_row_gb300 import build
+    build.build()
+    import paged_kv_cache_row_gb300 as p
+    return p.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "minisgl.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(minisgl_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    syms = declared_symbols()
+    for s in ("minisgl_store_kv", "minisgl_decode_attn", "minisgl_extend_attn"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import paged_kv_cache_row_gb300 as p
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"{s} declared in minisgl.h but not exported"
+    assert sorted(p.EXPORTED_SYMBOLS) == declared_symbols()
+
+
+def test_error_codes_on_host(lib):
+    import paged_kv_cache_row_gb300 as p
+    fake = 1 << 40  # never dereferenced: every call below fails validation first
+    d = p._PoolDesc(k_base=fake, v_base=fake, layer_stride=8 * 100 * 128, row_stride=8 * 128,
+                    num_layers=1, num_rows=100, num_kv_heads=8, head_dim=128, page_size=1,
+                    dtype=p.MINISGL_BF16)
+    ref = ctypes.byref
+    # NULL pool
+    assert lib.minisgl_store_kv(None, 0, fake, fake, 1024, 1024, fake, 4, None) == -1
+    # bad layer
+    assert lib.minisgl_store_kv(ref(d), 3, fake, fake, 1024, 1024, fake, 4, None) == -1
+    assert b"layer" in lib.minisgl_last_error()
+    # token stride below the row
+    assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 512, 1024, fake, 4, None) == -3
+    # dtype
+    bad = p._PoolDesc.from_buffer_copy(d)
+    bad.dtype = 7
+    assert lib.minisgl_decode_attn(ref(bad), 0, fake, 16, fake, 4, 32, 32, fake, 0.1, fake, fake,
+                                   1 << 20, 0, None) == -2
+    # head_dim
+    bad = p._PoolDesc.from_buffer_copy(d)
+    bad.head_dim = 96
+    assert lib.minisgl_decode_attn(ref(bad), 0, fake, 16, fake, 4, 32, 32, fake, 0.1, fake, fake,
+                                   1 << 20, 0, None) == -4
+    # group size 32 > 16, and a non-multiple head count
+    assert lib.minisgl_decode_attn(ref(d), 0, fake, 256, fake, 4, 32, 32, fake, 0.1, fake, fake,
+                                   1 << 20, 0, None) == -4
+    assert lib.minisgl_decode_attn(ref(d), 0, fake, 12, fake, 4, 32, 32, fake, 0.1, fake, fake,
+                                   1 << 20, 0, None) == -3
+    # workspace too small (needs 2 splits)
+    need = lib.minisgl_decode_workspace_bytes(4, 16, 8, 128, 2)
+    assert need > 0
+    assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 4, 32, 32, fake, 0.1, fake, fake,
+                                   need - 1, 0, None) == -6
+    # page table narrower than its width
+    assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 4, 16, 32, fake, 0.1, fake, fake,
+                                   need, 0, None) == -3
+    # extend: head_dim 64 unsupported, group 3 unsupported
+    bad = p._PoolDesc.from_buffer_copy(d)
+    bad.head_dim = 64
+    bad.row_stride = 8 * 64
+    assert lib.minisgl_extend_attn(ref(bad), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
+                                   0.1, fake, None) == -4
+    d3 = p._PoolDesc.from_buffer_copy(d)
+    d3.num_kv_heads = 2
+    d3.row_stride = 2 * 128
+    assert lib.minisgl_extend_attn(ref(d3), 0, fake, 6, fake, 2, 32, 32, fake, fake, fake, 10,
+                                   0.1, fake, None) == -4
+    # empty work is a no-op that touches nothing
+    assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 1024, 1024, fake, 0, None) == 0
+    assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 0, 32, 32, fake, 0.1, fake, fake,
+                                   0, 0, None) == 0
+
+
+def test_workspace_bytes_formula(lib):
+    def al(x):
+        return (x + 255) // 256 * 256
+    for B, Hq, Hk, d, S in [(4, 8, 2, 64, 2), (64, 16, 8, 128, 16), (256, 32, 8, 128, 17)]:
+        want = al(B * Hk * 4) + al(B * Hq * S * 4) + B * Hq * S * d * 4
+        assert lib.minisgl_decode_workspace_bytes(B, Hq, Hk, d, S) == want
+    assert lib.minisgl_decode_workspace_bytes(4, 8, 2, 64, 1) == 0
+    assert lib.minisgl_decode_workspace_bytes(4, 8, 2, 64, 257) == 0
+
+
+def test_kv_pool_bytes_golden():
+    import paged_kv_cache_row_gb300 as p
+    fx = json.load(open(os.path.join(ROOT, "tests", "golden", "kv_cache_size_example.json")))
+    got = p.kv_pool_bytes(fx["num_layers"], fx["num_kv_heads"], fx["head_dim"], fx["num_tokens"],
+                          fx["elem_bytes"])
+    assert got == fx["expected_bytes"]

@@ -1,0 +1,150 @@
+"""GPU parity of the tcgen05 causal extend kernel against the fp64 oracle.
+
+Cases span several 128-token KV tiles and several query blocks with ragged
+tails, every supported group size, empty and one-token prefixes and extends,
+radix-shared prefix rows and chunked-prefill batches whose later chunks read
+rows stored by earlier ones.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_row_gb300 as mk
+import workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_row_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def run_extend_case(case, check=True):
+    """store_kv + extend for every batch in order, against the oracle doing the same."""
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+    pool = mk.KVPool(pool_t)
+    orc = oracle.get()
+    outs = []
+    for b, (k, v, q) in zip(case.batches, per_batch):
+        mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+        o = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                                   b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+        torch.cuda.synchronize()
+        orc.store_kv(hk, hv, k.cpu(), v.cpu(), b.out_loc)
+        if check:
+            assert np.array_equal(gu.u16(pool_t[0, 0]), hk), "K pool differs from oracle store_kv"
+            ref = orc.extend(q.cpu(), hk, hv, b.page_table, b.cached_lens, b.extend_lens,
+                             case.sm_scale)
+            gu.check_attn(o, ref, f"{case.name} batch {len(outs)}")
+        outs.append(o)
+    assert mk.minisgl_debug_timeout_count() == 0, "a tensor-core kernel wait ran out"
+    return outs
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_extend_group_sizes(G):
+    Hkv = 2
+    case = workloads.make_extend_case(f"g{G}", num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128,
+                                      num_reqs=3, prefix_len=70, ext_lo=1, ext_hi=260, budget=4096,
+                                      seed=300 + G)
+    run_extend_case(case)
+
+
+def _manual_case(cached, ext, Hq=8, Hkv=2, seed=0):
+    """Requests with given cached / extend lengths, private rows, one batch."""
+    g = torch.Generator().manual_seed(seed)
+    lens = [c + e for c, e in zip(cached, ext)]
+    R = sum(lens) + 40
+    perm = torch.randperm(R - 2, generator=g).to(torch.int32)
+    W = workloads.align_up(max(lens + [1]))
+    pt = torch.full((len(lens), W), R - 1, dtype=torch.int32)
+    outs = []
+    off = 0
+    for r, n in enumerate(lens):
+        pt[r, :n] = perm[off:off + n]
+        outs.append(perm[off + cached[r]:off + n])
+        off += n
+    qo = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    qo[1:] = torch.cumsum(torch.tensor(ext, dtype=torch.int32), 0)
+    case = workloads.ExtendCase(name="manual", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+                                num_rows=R, prefix_rows=perm[:0], extend_lens=list(ext),
+                                sm_scale=1 / 128 ** 0.5, value_std=0.5, seed=seed)
+    case.batches.append(workloads.ExtendBatch(
+        req_ids=list(range(len(lens))), cached_lens=torch.tensor(cached, dtype=torch.int32),
+        extend_lens=torch.tensor(ext, dtype=torch.int32), q_offsets=qo, page_table=pt,
+        out_loc=torch.cat(outs).to(torch.int32)))
+    return case
+
+
+def test_extend_edge_lengths():
+    """No prefix, one-token extends, extends ending exactly on tile edges,
+    prefixes ending on tile edges, and an empty extend in the middle."""
+    cached = [0, 0, 128, 5, 127, 300, 0, 256]
+    ext = [1, 128, 1, 0, 129, 33, 257, 64]
+    run_extend_case(_manual_case(cached, ext, seed=41))
+
+
+def test_extend_prefix_shared_equals_private():
+    """Requests pointing at one set of radix-cache prefix rows give bit-identical
+    output to requests holding private copies of the same values."""
+    kw = dict(num_q_heads=16, num_kv_heads=4, head_dim=128, num_reqs=4, prefix_len=300,
+              ext_lo=50, ext_hi=200, budget=8192, seed=91)
+    shared = workloads.make_extend_case("shared", **kw)
+    private = workloads.make_extend_case("private", shared_prefix=False, **kw)
+    assert shared.extend_lens == private.extend_lens
+    pool_s, pb = workloads.make_extend_values(shared, DEV)
+    # private pool: same values at the private prefix rows and the new rows
+    pool_p = torch.zeros((2, 1, private.num_rows, 4, 128), dtype=torch.bfloat16, device=DEV)
+    for rs, rp in zip([shared.prefix_rows] * 4, private.prefix_rows_per_req):
+        pool_p[:, 0, rp.long().to(DEV)] = pool_s[:, 0, rs.long().to(DEV)]
+    outs = []
+    for case, pool_t in ((shared, pool_s), (private, pool_p)):
+        pool = mk.KVPool(pool_t)
+        o = []
+        for b, (k, v, q) in zip(case.batches, pb):
+            mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+            o.append(mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                                            b.extend_lens.to(DEV), b.q_offsets.to(DEV),
+                                            case.sm_scale))
+        outs.append(o)
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_extend_chunked_batches():
+    """Chunked prefill: a request cut by the token budget continues in the next
+    batch and reads the rows its first chunk stored."""
+    case = workloads.make_extend_case("chunked", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                                      num_reqs=5, prefix_len=100, ext_lo=60, ext_hi=300,
+                                      budget=256, seed=17)
+    assert len(case.batches) >= 3
+    assert any(int(b.cached_lens[0]) > 100 for b in case.batches[1:]), "expect a continued chunk"
+    run_extend_case(case)
+
+
+def test_extend_matches_decode_on_last_token():
+    """The last new token of an extend equals a decode of the same query over
+    the whole context (both kernels, same pool)."""
+    case = _manual_case([200, 37], [50, 91], Hq=16, Hkv=8, seed=5)
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    pool = mk.KVPool(pool_t)
+    b = case.batches[0]
+    k, v, q = per_batch[0]
+    mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+    o = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                               b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+    last = (b.q_offsets[1:] - 1).long()
+    qd = q[last.to(DEV)].contiguous()
+    seq = (b.cached_lens + b.extend_lens).to(DEV)
+    od = mk.minisgl_decode_attn(pool, 0, qd, b.page_table.to(DEV), seq, case.sm_scale)
+    torch.cuda.synchronize()
+    err = (o[last.to(DEV)].float() - od.float()).abs().max().item()
+    assert err <= 2 * gu.MAX_ABS

@@ -1,0 +1,115 @@
+"""Full-size parity for the five workloads, in the launch configuration the
+benchmark times: every layer is run, and outputs of sampled requests are
+checked against the oracle one by one; properties that hold at any size
+(store_kv bytes, CUDA-Graph padding output, finiteness) are checked on the
+whole output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_row_gb300 as mk
+import workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_row_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def run_decode_full(case, sample_reqs, sample_layers):
+    pool_t, k_new, v_new, q = workloads.make_decode_values(case, DEV)
+    pool = mk.KVPool(pool_t, case.page_size)
+    pt, sl, loc = case.page_table.to(DEV), case.seq_lens.to(DEV), case.out_loc.to(DEV)
+    # oracle inputs: the rows the sampled requests read, before any kernel runs
+    snaps = {}
+    rows = gu.request_rows(case.page_table, case.seq_lens, sample_reqs)
+    for l in sample_layers:
+        snaps[l] = gu.CompactPool(pool_t[0, l], pool_t[1, l], rows)
+    ws = mk.decode_workspace(case.batch, case.num_q_heads, pool)
+    outs = {}
+    for l in range(case.num_layers):  # the whole step, as the benchmark runs it
+        mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
+        o = mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, workspace=ws)
+        if l in sample_layers:
+            outs[l] = o.clone()
+    torch.cuda.synchronize()
+    for l in sample_layers:
+        assert torch.isfinite(outs[l][:case.num_real].float()).all()
+        # stored rows hold the new k/v exactly
+        assert torch.equal(pool_t[0, l][case.out_loc[:case.num_real].long().to(DEV)],
+                           k_new[l][:case.num_real])
+        assert torch.equal(pool_t[1, l][case.out_loc[:case.num_real].long().to(DEV)],
+                           v_new[l][:case.num_real])
+        cp = snaps[l]
+        real = [r for r in sample_reqs if r < case.num_real]
+        cp.store(k_new[l][real].cpu(), v_new[l][real].cpu(), case.out_loc[real])
+        ref, _ = gu.oracle_decode_requests(cp, q[l], case.page_table, case.seq_lens, real,
+                                           case.sm_scale)
+        gu.check_attn(outs[l][real], ref, f"{case.name} layer {l}")
+    return pool_t, k_new, v_new, outs
+
+
+def test_full_tiny_decode():
+    case = workloads.decode_tiny()
+    run_decode_full(case, list(range(case.batch)), [0])
+
+
+def test_full_qwen3_0p6b_decode():
+    case = workloads.decode_qwen3_0p6b()
+    run_decode_full(case, [0, 9, 31, 47, 63], [0, case.num_layers - 1])
+
+
+def test_full_llama3_8b_decode_with_padding():
+    case = workloads.decode_llama3_8b()
+    pool_t, k_new, v_new, outs = run_decode_full(case, [0, 57, 123, 199], [0, case.num_layers - 1])
+    D = case.dummy_row
+    G = case.num_q_heads // case.num_kv_heads
+    for l, o in outs.items():
+        # every padding request reads only the dummy row, whose V is the padding value
+        vd = v_new[l][case.num_real]            # [H_kv, d]
+        assert torch.equal(pool_t[1, l, D], vd)
+        exp = vd.repeat_interleave(G, dim=0)    # [H_q, d]
+        for r in range(case.num_real, case.batch):
+            assert torch.equal(o[r], exp), "padding request output != V[dummy]"
+
+
+def test_full_long_page64_decode():
+    case = workloads.decode_long_page64()
+    run_decode_full(case, [0, 11, 31], [0])
+
+
+def test_full_radix_shared_extend():
+    case = workloads.extend_radix_shared()
+    assert 2 <= len(case.batches) <= 5
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    host = (gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0]))  # ~0.2 GB: the whole pool
+    pool = mk.KVPool(pool_t)
+    orc = oracle.get()
+    for bi, (b, (k, v, q)) in enumerate(zip(case.batches, per_batch)):
+        assert b.total_tokens <= 8192
+        mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+        o = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                                   b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+        torch.cuda.synchronize()
+        orc.store_kv(host[0], host[1], k.cpu(), v.cpu(), b.out_loc)
+        assert torch.isfinite(o.float()).all()
+        # sampled tokens of the first and last request of the batch: new token t
+        # equals a decode of its query over logical tokens 0 .. C + t
+        gen = torch.Generator().manual_seed(bi)
+        for r in (0, len(b.req_ids) - 1):
+            C, E, a0 = int(b.cached_lens[r]), int(b.extend_lens[r]), int(b.q_offsets[r])
+            ts = sorted({0, E - 1, E // 2} | set(torch.randint(0, E, (5,), generator=gen).tolist()))
+            qs = q[[a0 + t for t in ts]].cpu()
+            pt = b.page_table[r:r + 1].repeat(len(ts), 1)
+            sl = torch.tensor([C + t + 1 for t in ts], dtype=torch.int32)
+            ref, _ = orc.decode(qs, host[0], host[1], pt, sl, case.sm_scale)
+            gu.check_attn(o[[a0 + t for t in ts]], ref, f"extend batch {bi} request {r}")
+    assert mk.minisgl_debug_timeout_count() == 0
