@@ -10,7 +10,7 @@
  *
  * Sources of the definitions (page title, section):
  *   [deep-dive]  "mini-sglang 架构深度解读" (mini-sglang architecture deep dive,
- *                tinymind.me): section 6.2 MHAKVCache layout, section 3
+ *                tinymind.me): section 6.2 MHAKVCache layout, section 3.6
  *                page-table figure, section 5 attention backends.
  *   [learn]      "doc-mini-sglang-learn" (mini-sglang learning notes): the
  *                paged KV pool chapter (pool shape, store_kv, dummy page,

@@ -12,7 +12,7 @@
  *     store_kv passage: one token row scattered per new token, by out_loc).
  *   - attention of one query over a request's context, gathered through its
  *     page_table row, which holds raw physical row numbers
- *     ("mini-sglang architecture deep dive", section 3 page-table figure and
+ *     ("mini-sglang architecture deep dive", section 3.6 TableManager page-table figure and
  *     section 5.3 PagedAttention figure; "mini-sglang-learn", page_table
  *     alignment passage).  The value is the textbook
  *         o = sum_j softmax_j(sm_scale * <q, K_j>) V_j
