@@ -174,6 +174,31 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         const int32_t *extend_lens, const int32_t *q_offsets,
                         int32_t total_q_tokens, float sm_scale, void *out, void *stream);
 
+/*
+ * Decode attention that allocates nothing (no counterpart in the pages; this
+ * is a convenience of this library).  Same arguments and results as
+ * minisgl_decode_attn minus the workspace: the split-KV scratch comes from a
+ * 32 MiB array in the library's own device memory instead of from the caller.
+ * For callers that cannot allocate device memory at run time -- an engine that
+ * has already given nearly all free HBM to its KV pool, code inside a host
+ * application that owns the device allocator, or a decode loop that cannot
+ * afford cudaMalloc/cudaFree synchronising the device.
+ *   - Every GPU on which the library is loaded holds the 32 MiB array until the
+ *     process exits.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress; make that first call
+ *     before any stream capture.
+ *   - Sizes whose scratch (minisgl_decode_workspace_bytes(..., 2)) exceeds
+ *     32 MiB are rejected with MINISGL_ERR_WORKSPACE and a message.
+ *   - All calls share the array: calls whose kernels can overlap on the GPU
+ *     (unordered streams) race and give wrong results.  Nothing in the array
+ *     needs to start at zero; every value a call reads, it wrote first.
+ */
+int minisgl_decode_attn_noalloc(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                                int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                                int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
+                                float sm_scale, void *out, int32_t split_tokens, void *stream);
+
 /* Message of the last error on the calling thread ("" if none). */
 const char *minisgl_last_error(void);
 

@@ -24,12 +24,13 @@ __all__ = [
     "KVPool", "minisgl_store_kv", "minisgl_decode_attn", "minisgl_extend_attn",
     "minisgl_decode_workspace_bytes", "minisgl_device_sm_count", "minisgl_debug_timeout_count",
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
+    "minisgl_decode_attn_noalloc",
 ]
 
 EXPORTED_SYMBOLS = [
     "minisgl_store_kv", "minisgl_decode_workspace_bytes", "minisgl_decode_attn",
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
-    "minisgl_debug_timeout_count",
+    "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc",
 ]
 
 MINISGL_BF16 = 1
@@ -69,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_decode_workspace_bytes.restype = sz
     lib.minisgl_decode_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, f32, vp, vp, sz, i32, vp]
     lib.minisgl_decode_attn.restype = ctypes.c_int
+    lib.minisgl_decode_attn_noalloc.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, f32, vp, i32, vp]
+    lib.minisgl_decode_attn_noalloc.restype = ctypes.c_int
     lib.minisgl_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, f32, vp, vp]
     lib.minisgl_extend_attn.restype = ctypes.c_int
     lib.minisgl_last_error.argtypes = []
@@ -205,6 +208,37 @@ def minisgl_decode_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: t
                                    page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
                                    float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
                                    split_tokens, _stream(stream)), "decode_attn")
+    return out
+
+
+def minisgl_decode_attn_noalloc(pool: KVPool, layer: int, q: torch.Tensor, page_table: torch.Tensor,
+                                seq_lens: torch.Tensor, sm_scale: float,
+                                out: Optional[torch.Tensor] = None, split_tokens: int = 0,
+                                stream=None) -> torch.Tensor:
+    """minisgl_decode_attn without a workspace, for callers that cannot allocate
+    device memory: the split-KV scratch comes from a fixed 32 MiB array inside
+    the library (one per GPU, shared by all calls, so calls must not overlap on
+    the GPU).  `out` must be given by a caller that cannot allocate; when it is
+    None this wrapper allocates it with torch for convenience."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16)
+    _need(page_table, "page_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, Hq, d = q.shape
+    if not q.is_contiguous() or d != pool.head_dim:
+        raise MinisglError("q must be contiguous [B, H_q, head_dim]")
+    if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if seq_lens.numel() != B or not seq_lens.is_contiguous():
+        raise MinisglError("seq_lens must be contiguous [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16)
+    _check(lib.minisgl_decode_attn_noalloc(ctypes.byref(pool.desc), layer, _ptr(q), Hq,
+                                           _ptr(page_table), B, page_table.stride(0),
+                                           page_table.shape[1], _ptr(seq_lens), float(sm_scale),
+                                           _ptr(out), split_tokens, _stream(stream)),
+           "decode_attn_noalloc")
     return out
 
 

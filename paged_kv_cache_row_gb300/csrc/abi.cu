@@ -73,6 +73,11 @@ int check_heads(int32_t hq, int32_t hkv, int max_group, const char *who) {
 }  // namespace
 
 namespace minisgl {
+int report_error(int code, const char *msg) {
+    g_err = msg;
+    return code;
+}
+
 int device_sm_count() {
     static int cached[64] = {0};
     int dev = 0;

@@ -55,6 +55,9 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s);
 
 int device_sm_count();
 
+// Sets the calling thread's minisgl_last_error() message and returns `code`.
+int report_error(int code, const char *msg);
+
 // Number of bounded waits that ran out in tensor-core kernels since load
 // (synchronous copy from a device counter).
 cudaError_t read_kernel_timeouts(unsigned int *count);
