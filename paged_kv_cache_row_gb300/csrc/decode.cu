@@ -39,18 +39,17 @@ namespace minisgl {
 namespace {
 
 constexpr int TILE = 16;  // tokens per warp tile
+constexpr int MAX_WARPS = 12;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-template <int D, int MROWS>
+template <int D>
 struct Cfg {
-    static constexpr int RB = D * 2;             // bytes of one head row
-    static constexpr int CPR = RB / 16;          // 16-byte chunks per row
-    static constexpr int KV_BYTES = TILE * RB;   // one K (or V) tile
-    static constexpr int Q_BYTES = MROWS * RB;   // the group's queries
-    static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-    static constexpr int NT = D / 8;             // n8 tiles along head_dim
-    static constexpr int KS = D / 16;            // k16 steps along head_dim
+    static constexpr int RB = D * 2;            // bytes of one head row
+    static constexpr int CPR = RB / 16;         // 16-byte chunks per row
+    static constexpr int KV_BYTES = TILE * RB;  // one K (or V) tile
+    static constexpr int KS = D / 16;           // k16 steps along head_dim (QK^T)
+    static constexpr int MT = D / 16;           // m16 tiles along head_dim (PV)
 };
 
 struct Cursor {
@@ -59,23 +58,37 @@ struct Cursor {
 
 __device__ __forceinline__ int clamp_len(int n, int w) { return min(max(n, 0), w); }
 
-// Swizzled byte offset of 16-byte chunk cc of row t inside a tile.
+// Swizzled byte offset of 16-byte chunk cc of row t inside a K or V tile.
 __device__ __forceinline__ uint32_t swz(int t, int cc, int rb) {
     return (uint32_t)(t * rb + ((cc ^ (t & 7)) << 4));
 }
 
+// Transpose an 8x8 b16 matrix held in the mma fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
 }  // namespace
 
-template <int D, int MROWS, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32)
-    decode_partial_kernel(const DecodeArgs a, const float scale_log2, const int prefix_bytes) {
-    using C = Cfg<D, MROWS>;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ int s_maxtiles;
-    int32_t *s_prefix = reinterpret_cast<int32_t *>(smem);
+// NG: n8 tiles of query heads (1 when the group has <= 8 heads, else 2).
+// The MMAs put the 16 tokens of a tile on M and the group's heads on N:
+//   S^T[tok, h] = K[tok, :] . Q[h, :]      (A = K tile, B = Q)
+//   O^T[c, h]  += V^T[c, tok] P^T[tok, h]  (A = V tile transposed, B = P^T)
+// so a group of 8 heads fills the MMA with no padding rows.
+template <int D, int NG, int STAGES>
+__global__ void __launch_bounds__(MAX_WARPS * 32, 1)
+    decode_partial_kernel(const DecodeArgs a, const float scale_log2, const int prefix_bytes,
+                          const int stage_bytes) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    int32_t *s_prefix = reinterpret_cast<int32_t *>(smem);  // [B + 1], then the longest stream
+    int32_t &s_maxtiles = s_prefix[a.batch + 1];
 
     const int B = a.batch, Hkv = a.num_kv_heads, Hq = a.num_q_heads, W = a.pt_width;
     const int G = Hq / Hkv;
+    const int WARPS = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ---- schedule: prefix over requests of (tiles per stream) * Hkv -------
@@ -111,7 +124,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     const __nv_bfloat16 *Kl = static_cast<const __nv_bfloat16 *>(a.k_layer);
     const __nv_bfloat16 *Vl = static_cast<const __nv_bfloat16 *>(a.v_layer);
     const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.q);
-    const uint32_t ring = smem_u32(smem + prefix_bytes) + warp * STAGES * C::STAGE_BYTES;
+    const uint32_t ring = smem_u32(smem + prefix_bytes) + warp * STAGES * stage_bytes;
 
     auto locate = [&](Cursor &c, int t) {
         int lo = 0, hi = B;  // largest r with prefix[r] <= t
@@ -144,8 +157,9 @@ __global__ void __launch_bounds__(WARPS * 32)
         const int row = __ldg(a.page_table + (int64_t)c.r * a.pt_stride + tok);
         return min(max(row, 0), a.num_rows - 1);
     };
+    // K and V rows of one tile (plus the group's queries when the tile opens a stream)
     auto issue = [&](int stage, const Cursor &c, int rows, bool with_q) {
-        const uint32_t st = ring + stage * C::STAGE_BYTES;
+        const uint32_t st = ring + stage * stage_bytes;
         const int64_t head = (int64_t)c.g * D;
 #pragma unroll
         for (int i = 0; i < TILE * C::CPR / 32; ++i) {
@@ -159,15 +173,9 @@ __global__ void __launch_bounds__(WARPS * 32)
             cp_async_16(st + C::KV_BYTES + off, Vl + e, bytes);
         }
         if (with_q) {
-#pragma unroll
-            for (int i = 0; i < MROWS * C::CPR / 32; ++i) {
-                const int ch = lane + 32 * i;
-                const int qi = ch / C::CPR, cc = ch % C::CPR;
-                const bool live = qi < G;
-                const __nv_bfloat16 *src =
-                    live ? Q + ((int64_t)c.r * Hq + c.g * G + qi) * D + cc * 8 : Q;
-                cp_async_16(st + 2 * C::KV_BYTES + swz(qi, cc, C::RB), src, live ? 16 : 0);
-            }
+            const __nv_bfloat16 *src = Q + ((int64_t)c.r * Hq + c.g * G) * D;
+            for (int ch = lane; ch < G * C::CPR; ch += 32)
+                cp_async_16(st + 2 * C::KV_BYTES + ch * 16, src + ch * 8, 16);
         }
     };
 
@@ -188,65 +196,78 @@ __global__ void __launch_bounds__(WARPS * 32)
             }
             cp_async_commit();
         }
-        int rows_next = (t0 + STAGES - 1 < t1) ? load_rows(pc) : -1;
+        // page-table rows two tiles ahead of the copies that need them
+        Cursor pl = pc;
+        int rows_a = -1, rows_b = -1;
+        if (t0 + STAGES - 1 < t1) {
+            rows_a = load_rows(pl);
+            if (t0 + STAGES < t1) {
+                advance(pl);
+                rows_b = load_rows(pl);
+            }
+        }
 
-        // consumer state
+        // consumer state: per head column e of n-tile n, running max m and lane-partial sum l
         int cur_r = -1, cur_g = 0, cur_nt = 0, cur_start = 0, first_j = 0, last_j = 0;
-        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-        float o[C::NT][4];
-        uint32_t qa[C::KS][4];
+        float m[NG][2], l[NG][2];
+        float o[C::MT][NG][4];
+        uint32_t qb[NG][C::KS][2];
 
         auto flush = [&]() {
-            float lr0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-            lr0 += __shfl_xor_sync(0xffffffffu, lr0, 2);
-            float lr1 = 0.f;
-            if (MROWS == 16) {
-                lr1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-                lr1 += __shfl_xor_sync(0xffffffffu, lr1, 2);
-            }
             const bool last = last_j == cur_nt - 1;
             const bool whole = first_j == 0 && last;
-            const int hl = lane >> 2, c2 = 2 * (lane & 3);
             const int s = whole ? 0 : (int)(seg - cur_start / P);
+            const int dr = lane >> 2;
 #pragma unroll
-            for (int half = 0; half < (MROWS == 16 ? 2 : 1); ++half) {
-                const int row = hl + 8 * half;
-                if (row >= G) continue;
-                const float lr = half ? lr1 : lr0, mr = half ? m1 : m0;
-                const float inv = 1.f / lr;
-                const int64_t hh = (int64_t)cur_r * Hq + cur_g * G + row;
-                if (whole) {
-                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + hh * D + c2;
+            for (int n = 0; n < NG; ++n)
 #pragma unroll
-                    for (int dt = 0; dt < C::NT; ++dt)
-                        *reinterpret_cast<uint32_t *>(dst + 8 * dt) =
-                            pack_bf16x2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
-                } else {
-                    float *dst = a.ws_o + (hh * a.max_splits + s) * D + c2;
+                for (int e = 0; e < 2; ++e) {
+                    float lt = l[n][e];
+                    lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+                    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+                    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+                    const int h = n * 8 + 2 * (lane & 3) + e;
+                    if (h >= G) continue;
+                    const float inv = 1.f / lt;
+                    const int64_t hh = (int64_t)cur_r * Hq + cur_g * G + h;
+                    if (whole) {
+                        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + hh * D + dr;
 #pragma unroll
-                    for (int dt = 0; dt < C::NT; ++dt)
-                        *reinterpret_cast<float2 *>(dst + 8 * dt) =
-                            make_float2(o[dt][2 * half] * inv, o[dt][2 * half + 1] * inv);
-                    if ((lane & 3) == 0) a.ws_lse[hh * a.max_splits + s] = (mr + __log2f(lr)) * LN2;
+                        for (int mt = 0; mt < C::MT; ++mt) {
+                            dst[16 * mt] = __float2bfloat16_rn(o[mt][n][e] * inv);
+                            dst[16 * mt + 8] = __float2bfloat16_rn(o[mt][n][2 + e] * inv);
+                        }
+                    } else {
+                        float *dst = a.ws_o + (hh * a.max_splits + s) * D + dr;
+#pragma unroll
+                        for (int mt = 0; mt < C::MT; ++mt) {
+                            dst[16 * mt] = o[mt][n][e] * inv;
+                            dst[16 * mt + 8] = o[mt][n][2 + e] * inv;
+                        }
+                        if (dr == 0) a.ws_lse[hh * a.max_splits + s] = (m[n][e] + __log2f(lt)) * LN2;
+                    }
                 }
-            }
             if (last && lane == 0) a.split_count[(int64_t)cur_r * Hkv + cur_g] = s + 1;
         };
 
         for (int t = t0; t < t1; ++t) {
             const int tp = t + STAGES - 1;
             if (tp < t1) {
-                issue((tp - t0) % STAGES, pc, rows_next, pc.j == 0);
+                issue((tp - t0) % STAGES, pc, rows_a, pc.j == 0);
                 if (tp + 1 < t1) {
                     advance(pc);
-                    rows_next = load_rows(pc);
+                    rows_a = rows_b;
+                    if (tp + 2 < t1) {
+                        advance(pl);
+                        rows_b = load_rows(pl);
+                    }
                 }
             }
             cp_async_commit();
             cp_async_wait<STAGES - 1>();
             __syncwarp();
 
-            const uint32_t st = ring + ((t - t0) % STAGES) * C::STAGE_BYTES;
+            const uint32_t st = ring + ((t - t0) % STAGES) * stage_bytes;
             if (cc.r != cur_r || cc.g != cur_g) {
                 if (cur_r >= 0) flush();
                 cur_r = cc.r;
@@ -254,100 +275,92 @@ __global__ void __launch_bounds__(WARPS * 32)
                 cur_nt = cc.nt;
                 cur_start = s_prefix[cc.r] + cc.g * cc.nt;
                 first_j = cc.j;
-                m0 = m1 = -INFINITY;
-                l0 = l1 = 0.f;
 #pragma unroll
-                for (int dt = 0; dt < C::NT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-                // query fragments (A operand, rows = heads of the group)
+                for (int n = 0; n < NG; ++n) {
+                    m[n][0] = m[n][1] = -INFINITY;
+                    l[n][0] = l[n][1] = 0.f;
+                }
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                    for (int n = 0; n < NG; ++n) o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
+                // Q as the B operand: b0 = Q[h][16ks + 2(l%4) + {0,1}], b1 = the same + 8
                 const uint32_t qs = st + 2 * C::KV_BYTES;
-                if (MROWS == 8) {
 #pragma unroll
-                    for (int ks = 0; ks < C::KS; ks += 2) {
-                        const int row = lane & 7, ch = 2 * ks + (lane >> 3);
-                        ldsm_x4(qs + swz(row, ch, C::RB), qa[ks][0], qa[ks][2], qa[ks + 1][0],
-                                qa[ks + 1][2]);
-                        qa[ks][1] = qa[ks][3] = qa[ks + 1][1] = qa[ks + 1][3] = 0u;
-                    }
-                } else {
+                for (int n = 0; n < NG; ++n) {
+                    const int h = n * 8 + (lane >> 2);
 #pragma unroll
                     for (int ks = 0; ks < C::KS; ++ks) {
-                        const int row = (lane & 7) + ((lane >> 3) & 1) * 8, ch = 2 * ks + (lane >> 4);
-                        ldsm_x4(qs + swz(row, ch, C::RB), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+                        uint32_t b0 = 0u, b1 = 0u;
+                        if (h < G) {
+                            const uint32_t ad = qs + h * C::RB + (16 * ks + 2 * (lane & 3)) * 2;
+                            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(b0) : "r"(ad));
+                            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(b1) : "r"(ad + 16));
+                        }
+                        qb[n][ks][0] = b0;
+                        qb[n][ks][1] = b1;
                     }
                 }
             }
 
-            // S = Q K^T for 16 tokens: two n8 tiles
-            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            // S^T = K Q^T for the tile's 16 tokens; two accumulator chains per n-tile
+            float sa[NG][2][4];
+#pragma unroll
+            for (int n = 0; n < NG; ++n)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) sa[n][c][0] = sa[n][c][1] = sa[n][c][2] = sa[n][c][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < C::KS; ++ks) {
-                const int tok = ((lane >> 4) << 3) + (lane & 7), ch = 2 * ks + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(st + swz(tok, ch, C::RB), b0, b1, b2, b3);
-                mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-            }
-            // online softmax (base 2), rows hl and hl+8
-            const int tok0 = cc.j * TILE + 2 * (lane & 3);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+                const int tok = (lane & 7) + ((lane >> 3) & 1) * 8, ch = 2 * ks + (lane >> 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(st + swz(tok, ch, C::RB), a0, a1, a2, a3);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                for (int n = 0; n < NG; ++n)
+                    mma_bf16_16816(sa[n][ks & 1], a0, a1, a2, a3, qb[n][ks][0], qb[n][ks][1]);
+            }
+            // online softmax per head column, base 2; this lane holds tokens
+            // dr and dr + 8 of the tile for heads 2(l%4) and 2(l%4)+1
+            const int tokA = cc.j * TILE + (lane >> 2);
+            const bool okA = tokA < cc.n, okB = tokA + 8 < cc.n;
+            uint32_t pb[NG][2];
+#pragma unroll
+            for (int n = 0; n < NG; ++n) {
+                float p[4];
+                float al[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool ok = tok0 + 8 * nt + e < cc.n;
-                    s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
-                    s[nt][2 + e] = ok ? s[nt][2 + e] * scale_log2 : -INFINITY;
-                    mx0 = fmaxf(mx0, s[nt][e]);
-                    mx1 = fmaxf(mx1, s[nt][2 + e]);
+                    const float x0 = okA ? (sa[n][0][e] + sa[n][1][e]) * scale_log2 : -INFINITY;
+                    const float x1 = okB ? (sa[n][0][2 + e] + sa[n][1][2 + e]) * scale_log2 : -INFINITY;
+                    float mx = fmaxf(x0, x1);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float mn = fmaxf(m[n][e], mx);
+                    al[e] = ex2(m[n][e] - mn);
+                    m[n][e] = mn;
+                    p[e] = ex2(x0 - mn);
+                    p[2 + e] = ex2(x1 - mn);
+                    l[n][e] = l[n][e] * al[e] + p[e] + p[2 + e];
                 }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            const float mn0 = fmaxf(m0, mx0);
-            const float al0 = ex2(m0 - mn0);
-            m0 = mn0;
-            float ps = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    s[nt][e] = ex2(s[nt][e] - mn0);
-                    ps += s[nt][e];
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    o[mt][n][0] *= al[0];
+                    o[mt][n][1] *= al[1];
+                    o[mt][n][2] *= al[0];
+                    o[mt][n][3] *= al[1];
                 }
-            l0 = l0 * al0 + ps;
-            float al1 = 1.f;
-            if (MROWS == 16) {
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn1 = fmaxf(m1, mx1);
-                al1 = ex2(m1 - mn1);
-                m1 = mn1;
-                float ps1 = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        s[nt][2 + e] = ex2(s[nt][2 + e] - mn1);
-                        ps1 += s[nt][2 + e];
-                    }
-                l1 = l1 * al1 + ps1;
+                // P^T as the B operand: transpose the two 8x8 token-by-head blocks
+                pb[n][0] = movmatrix_t(pack_bf16x2(p[0], p[1]));
+                pb[n][1] = movmatrix_t(pack_bf16x2(p[2], p[3]));
             }
-            // P as the A operand (rows = heads, k = the 16 tokens)
-            const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]);
-            const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]);
-            const uint32_t pa1 = MROWS == 16 ? pack_bf16x2(s[0][2], s[0][3]) : 0u;
-            const uint32_t pa3 = MROWS == 16 ? pack_bf16x2(s[1][2], s[1][3]) : 0u;
-            // O = O * alpha + P V
+            // O^T += V^T P^T
 #pragma unroll
-            for (int dt = 0; dt < C::NT; dt += 2) {
-                o[dt][0] *= al0; o[dt][1] *= al0; o[dt + 1][0] *= al0; o[dt + 1][1] *= al0;
-                if (MROWS == 16) {
-                    o[dt][2] *= al1; o[dt][3] *= al1; o[dt + 1][2] *= al1; o[dt + 1][3] *= al1;
-                }
-                const int tok = ((lane >> 3) & 1) * 8 + (lane & 7), ch = dt + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(st + C::KV_BYTES + swz(tok, ch, C::RB), b0, b1, b2, b3);
-                mma_bf16_16816(o[dt], pa0, pa1, pa2, pa3, b0, b1);
-                mma_bf16_16816(o[dt + 1], pa0, pa1, pa2, pa3, b2, b3);
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int tok = (lane & 7) + (lane >> 4) * 8, ch = 2 * mt + ((lane >> 3) & 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(st + C::KV_BYTES + swz(tok, ch, C::RB), a0, a1, a2, a3);
+#pragma unroll
+                for (int n = 0; n < NG; ++n) mma_bf16_16816(o[mt][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
             }
             last_j = cc.j;
             if (t + 1 < t1) advance(cc);
@@ -392,14 +405,45 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeArgs a) {
 
 namespace {
 
+struct SmemInfo {
+    int optin;     // dynamic + static shared memory one CTA may use
+    int per_sm;    // shared memory of one SM
+    int reserved;  // shared memory the system reserves per CTA
+};
+
+SmemInfo smem_info() {
+    static std::mutex mu;
+    static SmemInfo cache[64];
+    static bool have[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && have[dev]) return cache[dev];
+    SmemInfo si{48 * 1024, 48 * 1024, 0};
+    cudaDeviceGetAttribute(&si.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&si.per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&si.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (dev >= 0 && dev < 64) {
+        cache[dev] = si;
+        have[dev] = true;
+    }
+    return si;
+}
+
 struct LaunchCache {
     std::mutex mu;
-    struct Entry { const void *fn; int dev; size_t smem; int blocks; };
+    struct Entry { const void *fn; int dev; size_t smem; int threads; int blocks; };
     Entry e[64];
     int n = 0;
+    struct Attr { const void *fn; int dev; };
+    Attr a[64];
+    int na = 0;
 };
 LaunchCache g_cache;
 
+// CTAs per SM for `kernel` at this block size and dynamic shared memory.  The
+// kernel's dynamic shared-memory limit is raised to the device maximum once
+// per device, so launches with any smaller size stay valid.
 template <typename K>
 int blocks_per_sm(K kernel, int threads, size_t smem) {
     int dev = 0;
@@ -407,32 +451,62 @@ int blocks_per_sm(K kernel, int threads, size_t smem) {
     std::lock_guard<std::mutex> lk(g_cache.mu);
     for (int i = 0; i < g_cache.n; ++i)
         if (g_cache.e[i].fn == (const void *)kernel && g_cache.e[i].dev == dev &&
-            g_cache.e[i].smem == smem)
+            g_cache.e[i].smem == smem && g_cache.e[i].threads == threads)
             return g_cache.e[i].blocks;
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    bool attr = false;
+    for (int i = 0; i < g_cache.na; ++i)
+        if (g_cache.a[i].fn == (const void *)kernel && g_cache.a[i].dev == dev) attr = true;
+    if (!attr) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        const int dyn_max = smem_info().optin - (int)fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) !=
+            cudaSuccess) {
+            cudaGetLastError();  // do not leave the failure for the next caller to find
+            return 0;
+        }
+        if (g_cache.na < 64) g_cache.a[g_cache.na++] = {(const void *)kernel, dev};
+    }
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
         nb = 0;
-    if (g_cache.n < 64) g_cache.e[g_cache.n++] = {(const void *)kernel, dev, smem, nb};
+    }
+    if (g_cache.n < 64) g_cache.e[g_cache.n++] = {(const void *)kernel, dev, smem, threads, nb};
     return nb;
 }
 
-template <int D, int MROWS>
+template <int D, int NG, int STAGES>
 cudaError_t launch_cfg(const DecodeArgs &a, cudaStream_t s) {
-    constexpr int WARPS = 4, STAGES = 4;
-    using C = Cfg<D, MROWS>;
-    const int prefix_bytes = (((a.batch + 1) * 4) + 1023) / 1024 * 1024;
-    const size_t smem = (size_t)prefix_bytes + (size_t)WARPS * STAGES * C::STAGE_BYTES;
-    auto kern = decode_partial_kernel<D, MROWS, WARPS, STAGES>;
-    const int nb = blocks_per_sm(kern, WARPS * 32, smem);
+    using C = Cfg<D>;
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const int prefix_bytes = (((a.batch + 2) * 4) + 1023) / 1024 * 1024;
+    const int stage_bytes = ((2 * C::KV_BYTES + G * C::RB) + 127) / 128 * 128;
+    // As many warps per SM as shared memory allows (more warps hide more
+    // latency), as two CTAs of at most CTA_WARPS warps when they fit.
+    constexpr int CTA_WARPS = 6;
+    const SmemInfo si = smem_info();
+    const int per_warp = STAGES * stage_bytes;
+    const int fixed = prefix_bytes + si.reserved;
+    int warps = (si.per_sm - 2 * fixed) / per_warp / 2;
+    if (warps < 1) warps = (si.per_sm - fixed) / per_warp;  // one CTA per SM
+    if (warps > CTA_WARPS) warps = CTA_WARPS;
+    while (warps > 0 && prefix_bytes + warps * per_warp > si.optin) --warps;
+    if (warps < 1) return cudaErrorInvalidConfiguration;
+    const size_t smem = (size_t)prefix_bytes + (size_t)warps * per_warp;
+    auto kern = decode_partial_kernel<D, NG, STAGES>;
+    const int nb = blocks_per_sm(kern, warps * 32, smem);
     if (nb <= 0) return cudaErrorInvalidConfiguration;
     // never more warps than tiles could exist
     const int64_t max_tiles = (int64_t)a.batch * a.num_kv_heads * ((a.pt_width + TILE - 1) / TILE);
     int64_t grid = (int64_t)device_sm_count() * nb;
-    const int64_t need = (max_tiles + WARPS - 1) / WARPS;
+    const int64_t need = (max_tiles + warps - 1) / warps;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, WARPS * 32, smem, s>>>(a, a.sm_scale * LOG2E, prefix_bytes);
+    kern<<<(unsigned)grid, warps * 32, smem, s>>>(a, a.sm_scale * LOG2E, prefix_bytes, stage_bytes);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_merge_kernel<D><<<a.batch * a.num_kv_heads, D, 0, s>>>(a);
@@ -444,8 +518,8 @@ cudaError_t launch_cfg(const DecodeArgs &a, cudaStream_t s) {
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
     const int G = a.num_q_heads / a.num_kv_heads;
-    if (a.head_dim == 128) return G <= 8 ? launch_cfg<128, 8>(a, s) : launch_cfg<128, 16>(a, s);
-    return G <= 8 ? launch_cfg<64, 8>(a, s) : launch_cfg<64, 16>(a, s);
+    if (a.head_dim == 128) return G <= 8 ? launch_cfg<128, 1, 2>(a, s) : launch_cfg<128, 2, 2>(a, s);
+    return G <= 8 ? launch_cfg<64, 1, 2>(a, s) : launch_cfg<64, 2, 2>(a, s);
 }
 
 }  // namespace minisgl
