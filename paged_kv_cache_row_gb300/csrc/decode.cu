@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
     const int G = Hq / Hkv;
     const int WARPS = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_launch_dependents();
 
     // ---- schedule: prefix over requests of (tiles per stream) * Hkv -------
     if (warp == 0) {
@@ -372,35 +374,59 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
     }
 }
 
-// One CTA per (request, KV head); thread c owns channel c of every head of
-// the group.  Streams that one warp finished are left alone (their bf16
-// output is final); empty requests get zeros.
+// One warp per (request, query head).  Streams that one warp of the partial
+// kernel finished (split count 1) already hold their final bf16 output and are
+// skipped; empty requests get zeros.  Lane s holds the weight of split s (32 at
+// a time); every lane owns D/32 consecutive channels.
 template <int D>
-__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    constexpr int CPL = D / 32;  // channels per lane
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
-    const int r = blockIdx.x / Hkv, g = blockIdx.x - r * Hkv;
-    const int c = threadIdx.x;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+    const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (wid >= a.batch * Hq) return;
+    const int r = wid / Hq, h = wid - r * Hq, g = h / G;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (int64_t)wid * D + lane * CPL;
     const int n = min(max(__ldg(a.seq_lens + r), 0), a.pt_width);
     if (n == 0) {
-        for (int i = 0; i < G; ++i)
-            out[((int64_t)r * Hq + g * G + i) * D + c] = __float2bfloat16_rn(0.f);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) out[c] = __float2bfloat16_rn(0.f);
         return;
     }
     const int S = min(a.split_count[(int64_t)r * Hkv + g], a.max_splits);
     if (S <= 1) return;
-    for (int i = 0; i < G; ++i) {
-        const int64_t base = ((int64_t)r * Hq + g * G + i) * a.max_splits;
-        float M = -INFINITY;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, a.ws_lse[base + s]);
-        float tot = 0.f, acc = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float w = __expf(a.ws_lse[base + s] - M);
-            tot += w;
-            acc += w * a.ws_o[(base + s) * D + c];
+    const int64_t base = (int64_t)wid * a.max_splits;
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < S; s0 += 32)
+        if (s0 + lane < S) M = fmaxf(M, a.ws_lse[base + s0 + lane]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    float tot = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+        const float w = s0 + lane < S ? __expf(a.ws_lse[base + s0 + lane] - M) : 0.f;
+        tot += w;
+        const int ns = min(32, S - s0);
+        for (int k = 0; k < ns; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            const float *src = a.ws_o + (base + s0 + k) * D + lane * CPL;
+#pragma unroll
+            for (int c = 0; c < CPL; c += 2) {
+                const float2 v = *reinterpret_cast<const float2 *>(src + c);
+                acc[c] += wk * v.x;
+                acc[c + 1] += wk * v.y;
+            }
         }
-        out[((int64_t)r * Hq + g * G + i) * D + c] = __float2bfloat16_rn(acc / tot);
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const float inv = 1.f / tot;
+#pragma unroll
+    for (int c = 0; c < CPL; c += 2)
+        *reinterpret_cast<uint32_t *>(out + c) = pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
 }
 
 namespace {
@@ -506,11 +532,11 @@ cudaError_t launch_cfg(const DecodeArgs &a, cudaStream_t s) {
     const int64_t need = (max_tiles + warps - 1) / warps;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, warps * 32, smem, s>>>(a, a.sm_scale * LOG2E, prefix_bytes, stage_bytes);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(warps * 32), smem, s, a,
+                               a.sm_scale * LOG2E, prefix_bytes, stage_bytes);
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<D><<<a.batch * a.num_kv_heads, D, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_merge_kernel<D>, dim3((a.batch * a.num_q_heads + 3) / 4), dim3(128), 0,
+                      s, a);
 }
 
 }  // namespace

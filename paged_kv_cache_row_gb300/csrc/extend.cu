@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int G = 1 << log2g;
     const int TQ = ROWS >> log2g;  // new tokens per work item
 
+    pdl_wait();
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(kv_full(s), 128);
@@ -179,16 +181,44 @@ __global__ void __launch_bounds__(THREADS, 1)
 
         if (warp >= 4 && warp < 8) {
             // ---------------- producer: Q once, then K/V tiles ----------------
+            // Thread pt copies 16-byte chunk cc of rows tb*16 .. tb*16+15 of each
+            // 128-row tile (16 threads cover one 256-byte row).  The page-table
+            // entries of the next tile are fetched while this tile's copies go out.
             const int pt = threadIdx.x - 128;
-            const int cc = pt & 15, row0 = pt >> 4;  // chunk of a row; rows row0 + 8k
+            const int cc = pt & 15, tb = pt >> 4;
             const int32_t *ptab = a.page_table + (int64_t)r * a.pt_stride;
+            auto fetch_rows = [&](int j, int (&rows)[16]) {
+                const int p0 = j * ROWS + tb * 16;
+                if (p0 + 16 <= n_vis && ((reinterpret_cast<uintptr_t>(ptab + p0) & 15) == 0)) {
+                    const int4 *src = reinterpret_cast<const int4 *>(ptab + p0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int4 v = __ldg(src + q);
+                        rows[4 * q + 0] = v.x;
+                        rows[4 * q + 1] = v.y;
+                        rows[4 * q + 2] = v.z;
+                        rows[4 * q + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) rows[k] = p0 + k < n_vis ? __ldg(ptab + p0 + k) : -1;
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    rows[k] = rows[k] < 0 ? -1 : min(rows[k], a.num_rows - 1);
+            };
+            int rows_cur[16], rows_nxt[16];
+            fetch_rows(0, rows_nxt);
             for (int j = 0; j < nkv; ++j) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) rows_cur[k] = rows_nxt[k];
+                if (j + 1 < nkv) fetch_rows(j + 1, rows_nxt);
                 const uint32_t it = kv_iter + j, st = it & 1;
                 if (it >= STAGES) wait(kv_empty(st), ((it >> 1) - 1) & 1);
                 if (j == 0) {
-#pragma unroll 4
+#pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        const int i = row0 + 8 * k;
+                        const int i = tb * 16 + k;
                         const int t = t_first + (i >> log2g);
                         const bool live = t <= t_last;
                         const __nv_bfloat16 *src =
@@ -198,12 +228,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 const uint32_t sK = sKV + st * 2 * TILE_BYTES, sV = sK + TILE_BYTES;
-#pragma unroll 4
+#pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const int tok = row0 + 8 * k;
-                    const int pos = j * ROWS + tok;
-                    int row = -1;
-                    if (pos < n_vis) row = min(max(__ldg(ptab + pos), 0), a.num_rows - 1);
+                    const int tok = tb * 16 + k;
+                    const int row = rows_cur[k];
                     const int64_t e = (int64_t)max(row, 0) * a.row_stride + (int64_t)g * D + cc * 8;
                     const int bytes = row >= 0 ? 16 : 0;
                     const uint32_t o = sw128(tok, cc);
@@ -396,8 +424,8 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
     int64_t grid = device_sm_count();
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
-    extend_kernel<<<(unsigned)grid, THREADS, smem, s>>>(a, a.sm_scale * LOG2E, log2g);
-    return cudaGetLastError();
+    return launch_pdl(extend_kernel, dim3((unsigned)grid), dim3(THREADS), smem, s, a,
+                      a.sm_scale * LOG2E, log2g);
 }
 
 cudaError_t read_kernel_timeouts(unsigned int *count) {

@@ -7,6 +7,25 @@
 
 namespace minisgl {
 
+// Launch with programmatic stream serialization, so this kernel's launch and
+// prologue overlap the tail of the previous kernel in the stream; the kernel
+// itself calls griddepcontrol.wait before touching global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct StoreArgs {
     void *k_layer, *v_layer;      // layer base of K / V in the pool
     int64_t row_stride;           // elements between pool rows

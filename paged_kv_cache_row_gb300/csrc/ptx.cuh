@@ -64,6 +64,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// ---- programmatic dependent launch -----------------------------------------
+// Wait until the grid this launch depends on has finished and its memory is
+// visible (a no-op for launches without the programmatic-serialization
+// attribute).  Every kernel calls it before its first global read.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Allow the next kernel in the stream to be scheduled; it still waits for
+// this grid to finish before it reads anything.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ---- 16-byte global loads/stores -----------------------------------------
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
     uint4 v;

@@ -17,6 +17,8 @@
 namespace minisgl {
 
 __global__ void __launch_bounds__(256) store_kv_kernel(StoreArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int chunks = a.row_elems / 8;                  // 16-byte chunks per row
     const int64_t per_tok = 2LL * chunks;                // K then V
     const int64_t total = (int64_t)a.n_tokens * per_tok;
@@ -43,8 +45,7 @@ cudaError_t launch_store_kv(const StoreArgs &a, cudaStream_t s) {
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)device_sm_count() * 16;
     if (blocks > cap) blocks = cap;
-    store_kv_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(store_kv_kernel, dim3((unsigned)blocks), dim3(256), 0, s, a);
 }
 
 }  // namespace minisgl
