@@ -11,27 +11,32 @@
 //     out[q_off[r]+t, h] = sum_{j <= C_r+t} softmax_j(sm_scale <q, K[pt[r,j], g]>) V[pt[r,j], g].
 //
 // Design (GB300, one CTA per SM, persistent):
-//   * Work item = (request, KV head g, block of TQ = 128/G new tokens).  The
-//     128 MMA rows are the (token, head) pairs of the block: the G query
-//     heads that share KV head g ride in the same tile, so each gathered K/V
-//     tile feeds G heads.
-//   * Producer warps 4-7 gather 128-token K and V tiles through page_table
-//     with 16-byte cp.async into the 128-byte-swizzled layout the tensor
-//     core reads (K as a K-major B operand, V as an MN-major B operand), two
-//     stages deep; completion is tracked by mbarriers
-//     (cp.async.mbarrier.arrive).
-//   * Warp 8 (one lane) issues tcgen05.mma: S = Q K^T (M=N=128, K=16 steps)
-//     into one of two S buffers in TMEM, then O += P V into a TMEM O buffer,
-//     and signals completions with tcgen05.commit.
-//   * Softmax warps 0-3: thread i owns TMEM lane (= MMA row) i.  It reads its
-//     S row, applies the causal limit C + t, keeps a running max m and sum l
-//     (base 2), writes P = 2^(s - m) as bf16 into shared memory for the PV
-//     MMA, and rescales its O row in TMEM only when the max has grown by
-//     more than 2^8 (the final O / l is unchanged by when the rescale
-//     happens).  Epilogue: O / l -> bf16 -> global.
+//   * Work item = (request, KV head g, block of 2*TQ new tokens), TQ = 128/G.
+//     The block is two query tiles A and B of 128 MMA rows each; a row is a
+//     (token, head) pair, so the G query heads that share KV head g ride in
+//     the same tile and every gathered K/V tile feeds 2*128 rows.
+//   * Producer warps 8-11 gather 128-token K and V tiles through page_table
+//     with 16-byte cp.async into the 128-byte-swizzled layout the tensor core
+//     reads (K as a K-major B operand, V as an MN-major B operand), two
+//     stages deep; completion is tracked by mbarriers (cp.async.mbarrier.arrive).
+//   * Warp 12 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
+//     (M = N = 128) into tensor memory; O_X += P_X V with P_X read from
+//     tensor memory.  The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//     keeps the tensor core on one tile while the other tile's softmax runs.
+//   * Softmax warpgroups 0 (warps 0-3, tile A) and 1 (warps 4-7, tile B):
+//     thread i owns TMEM lane (= MMA row) i of its tile.  It reads its S row
+//     (two passes of 32-column chunks: maximum, then exponentials), applies
+//     the causal limit C + t, keeps a running max m and sum l (base 2), and
+//     writes P = 2^(s - m) as bf16 back into the first 64 columns of its S
+//     row, where the PV MMA reads it.  O_X is rescaled in tensor memory only
+//     when the max has grown by more than 2^8 (the final O / l does not
+//     depend on when the rescale happens).  Epilogue: O / l -> bf16 -> global.
+//   * Tensor memory (512 columns): S_A 0-127, S_B 128-255, O_A 256-383,
+//     O_B 384-511.  Shared memory: Q_A, Q_B (32 KB each), two K/V stages
+//     (64 KB each).
 //   * Every mbarrier wait is bounded in time; a wait that runs out sets a
 //     flag, the kernel finishes without further waiting (its output is then
-//     garbage) and the device counter minisgl_timeouts is increased.
+//     garbage) and a device counter of such events is increased.
 #include <mutex>
 
 #include "kernels.h"
@@ -44,23 +49,25 @@ __device__ unsigned int g_kernel_timeouts = 0;
 namespace {
 
 constexpr int D = 128;
-constexpr int ROWS = 128;                 // MMA M and KV tile length
+constexpr int ROWS = 128;                 // rows of a query tile, tokens of a KV tile
 constexpr int TILE_BYTES = ROWS * D * 2;  // 32 KB: 128 rows of 256 bytes
 constexpr int HALF = TILE_BYTES / 2;      // one 64-column swizzle region
-constexpr int OFF_Q = 0;
-constexpr int OFF_P = TILE_BYTES;
+constexpr int OFF_Q = 0;                  // Q_A, then Q_B
 constexpr int OFF_KV = 2 * TILE_BYTES;    // stage s: K at +2s*TILE, V at +(2s+1)*TILE
 constexpr int STAGES = 2;
 constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE_BYTES;  // 192 KB
-constexpr int OFF_TMEM_SLOT = OFF_BAR + 96;
-constexpr int OFF_PREFIX = OFF_BAR + 128;
-constexpr int THREADS = 288;              // 4 softmax + 4 producer + 1 MMA warp
-constexpr int MMA_WARP = 8;
+constexpr int OFF_TMEM_SLOT = OFF_BAR + 192;
+constexpr int OFF_PREFIX = OFF_BAR + 256;
+constexpr int THREADS = 416;              // 2 softmax warpgroups + 4 producer warps + 1 MMA warp
+constexpr int PRODUCER_WARP0 = 8;
+constexpr int MMA_WARP = 12;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // SM cycles (about 2 s)
+
+__device__ __forceinline__ uint32_t col_s(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return x ? 384u : 256u; }
 
 // byte offset of 16-byte chunk cc (0..15) of row `row` in a 128 x 256 B tile
 // stored as two 128-byte-swizzled 64-column regions
@@ -92,19 +99,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ int s_abort;
     const uint32_t sb = smem_u32(base);
-    const uint32_t sQ = sb + OFF_Q, sP = sb + OFF_P, sKV = sb + OFF_KV;
+    const uint32_t sQ = sb + OFF_Q, sKV = sb + OFF_KV;
     const uint32_t bar = sb + OFF_BAR;
     auto kv_full = [&](int s) { return bar + 8 * s; };
     auto kv_empty = [&](int s) { return bar + 16 + 8 * s; };
-    auto s_full = [&](int b) { return bar + 32 + 8 * b; };
-    const uint32_t p_full = bar + 48, pv_done = bar + 56, fin = bar + 64;
+    auto s_full = [&](int x) { return bar + 32 + 8 * x; };
+    auto p_full = [&](int x) { return bar + 48 + 8 * x; };
+    auto pv_done = [&](int x) { return bar + 64 + 8 * x; };
+    const uint32_t fin = bar + 80;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + OFF_TMEM_SLOT);
     int32_t *s_prefix = reinterpret_cast<int32_t *>(base + OFF_PREFIX);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = a.batch, Hkv = a.num_kv_heads, Hq = a.num_q_heads, W = a.pt_width;
     const int G = 1 << log2g;
-    const int TQ = ROWS >> log2g;  // new tokens per work item
+    const int TQ = ROWS >> log2g;  // new tokens per query tile
+    const int TQ2 = 2 * TQ;        // new tokens per work item
 
     pdl_wait();
     pdl_launch_dependents();
@@ -113,10 +123,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(kv_full(s), 128);
             mbar_init(kv_empty(s), 1);
         }
-        mbar_init(s_full(0), 1);
-        mbar_init(s_full(1), 1);
-        mbar_init(p_full, 128);
-        mbar_init(pv_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), 128);
+            mbar_init(pv_done(x), 1);
+        }
         mbar_init(fin, 1);
         fence_mbar_init();
         s_abort = 0;
@@ -125,8 +136,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
-    // items per request: ceil(E / TQ) blocks times Hkv heads, prefix in shared memory
-    if (warp == 4) {
+    // items per request: ceil(E / TQ2) blocks times Hkv heads, prefix in shared memory
+    if (warp == PRODUCER_WARP0) {
         int carry = 0;
         if (lane == 0) s_prefix[0] = 0;
         for (int b0 = 0; b0 < B; b0 += 32) {
@@ -135,7 +146,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (r < B) {
                 const int c = min(max(__ldg(a.cached_lens + r), 0), W);
                 const int e = min(max(__ldg(a.extend_lens + r), 0), W - c);
-                v = ((e + TQ - 1) / TQ) * Hkv;
+                v = ((e + TQ2 - 1) / TQ2) * Hkv;
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -160,7 +171,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t idesc_qk = idesc_bf16_f32(ROWS, ROWS, false);
     const uint32_t idesc_pv = idesc_bf16_f32(ROWS, D, true);
 
-    uint32_t kv_iter = 0;  // KV tiles this CTA has gone through (all roles count alike)
+    // Running counts shared by all roles: KV tiles, and tiles processed per query tile.
+    uint32_t kv_iter = 0, cnt_a = 0, cnt_b = 0;
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         int lo = 0, hi = B;
         while (hi - lo > 1) {
@@ -174,17 +186,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int C = min(max(__ldg(a.cached_lens + r), 0), W);
         const int E = min(max(__ldg(a.extend_lens + r), 0), W - C);
         const int qoff = __ldg(a.q_offsets + r);
-        const int t_first = qb * TQ;
-        const int t_last = min(t_first + TQ, E) - 1;
-        const int n_vis = C + t_last + 1;  // KV positions this block can see
-        const int nkv = (n_vis + ROWS - 1) / ROWS;
+        const int t0 = qb * TQ2;                    // first new token of tile A
+        const int ta_last = min(t0 + TQ, E) - 1;    // last live token of tile A
+        const bool live_b = t0 + TQ < E;
+        const int tb_last = live_b ? min(t0 + TQ2, E) - 1 : ta_last;
+        const int nkv_a = (C + ta_last + 1 + ROWS - 1) / ROWS;
+        const int nkv_b = live_b ? (C + tb_last + 1 + ROWS - 1) / ROWS : 0;
+        const int nkv = max(nkv_a, nkv_b);
+        const int n_vis = C + tb_last + 1;         // KV positions the item can see
 
-        if (warp >= 4 && warp < 8) {
-            // ---------------- producer: Q once, then K/V tiles ----------------
+        if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
+            // ---------------- producer: Q_A, Q_B once, then K/V tiles ----------------
             // Thread pt copies 16-byte chunk cc of rows tb*16 .. tb*16+15 of each
             // 128-row tile (16 threads cover one 256-byte row).  The page-table
             // entries of the next tile are fetched while this tile's copies go out.
-            const int pt = threadIdx.x - 128;
+            const int pt = threadIdx.x - PRODUCER_WARP0 * 32;
             const int cc = pt & 15, tb = pt >> 4;
             const int32_t *ptab = a.page_table + (int64_t)r * a.pt_stride;
             auto fetch_rows = [&](int j, int (&rows)[16]) {
@@ -217,15 +233,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (it >= STAGES) wait(kv_empty(st), ((it >> 1) - 1) & 1);
                 if (j == 0) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int i = tb * 16 + k;
-                        const int t = t_first + (i >> log2g);
-                        const bool live = t <= t_last;
-                        const __nv_bfloat16 *src =
-                            live ? Q + ((int64_t)(qoff + t) * Hq + g * G + (i & (G - 1))) * D + cc * 8
-                                 : Q;
-                        cp_async_16(sQ + sw128(i, cc), src, live ? 16 : 0);
-                    }
+                    for (int x = 0; x < 2; ++x)
+#pragma unroll 4
+                        for (int k = 0; k < 16; ++k) {
+                            const int i = tb * 16 + k;
+                            const int t = t0 + x * TQ + (i >> log2g);
+                            const bool live = t <= (x ? tb_last : ta_last) && (x == 0 || live_b);
+                            const __nv_bfloat16 *src =
+                                live ? Q + ((int64_t)(qoff + t) * Hq + g * G + (i & (G - 1))) * D + cc * 8
+                                     : Q;
+                            cp_async_16(sQ + x * TILE_BYTES + sw128(i, cc), src, live ? 16 : 0);
+                        }
                 }
                 const uint32_t sK = sKV + st * 2 * TILE_BYTES, sV = sK + TILE_BYTES;
 #pragma unroll
@@ -244,143 +262,160 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else if (warp == MMA_WARP) {
             // ---------------- MMA issuer ----------------
             if (lane == 0) {
-                // S(j) is issued one tile ahead of PV(j-1), so the S MMA of the next
-                // tile runs while the softmax warps work on the current one.
-                for (int j = 0; j <= nkv; ++j) {
-                    if (j < nkv) {
-                        const uint32_t it = kv_iter + j, st = it & 1;
-                        wait(kv_full(st), (it >> 1) & 1);
-                        fence_proxy_async_smem();
-                        tc_fence_after();
-                        const uint32_t sK = sKV + st * 2 * TILE_BYTES;
-                        const uint32_t dS = tmem + ((it & 1) ? COL_S1 : COL_S0);
+                auto issue_s = [&](int x, int j) {  // S_X(j) = Q_X K(j)^T
+                    const uint32_t sK = sKV + ((kv_iter + j) & 1) * 2 * TILE_BYTES;
+                    const uint32_t qx = sQ + x * TILE_BYTES;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t ad = smem_desc_sw128(sQ + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(sK + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-                            tc_mma_bf16(dS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(s_full(it & 1));
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(qx + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(sK + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
+                        tc_mma_bf16(tmem + col_s(x), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    if (j > 0) {
-                        const int jj = j - 1;
-                        const uint32_t itp = kv_iter + jj, st = itp & 1;
-                        wait(p_full, itp & 1);
-                        tc_fence_after();
-                        const uint32_t sV = sKV + st * 2 * TILE_BYTES + TILE_BYTES;
+                    tc_commit(s_full(x));
+                };
+                auto issue_pv = [&](int x, int j, uint32_t cnt) {  // O_X += P_X(j) V(j)
+                    wait(p_full(x), (cnt + j) & 1);
+                    tc_fence_after();
+                    const uint32_t sV = sKV + ((kv_iter + j) & 1) * 2 * TILE_BYTES + TILE_BYTES;
 #pragma unroll
-                        for (int kk = 0; kk < ROWS / 16; ++kk) {
-                            const uint64_t ad = smem_desc_sw128(sP + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(sV + kk * 2048, HALF, 1024);
-                            tc_mma_bf16(tmem + COL_O, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit(pv_done);
-                        tc_commit(kv_empty(st));
+                    for (int kk = 0; kk < ROWS / 16; ++kk) {
+                        const uint64_t bd = smem_desc_sw128(sV + kk * 2048, HALF, 1024);
+                        tc_mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bd, idesc_pv,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(pv_done(x));
+                };
+                auto wait_kv = [&](int j) {
+                    wait(kv_full((kv_iter + j) & 1), ((kv_iter + j) >> 1) & 1);
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                };
+                wait_kv(0);
+                issue_s(0, 0);
+                if (nkv_b > 0) issue_s(1, 0);
+                for (int j = 0; j < nkv; ++j) {
+                    bool next_ready = false;
+                    if (j < nkv_a) issue_pv(0, j, cnt_a);
+                    if (j + 1 < nkv_a) {
+                        wait_kv(j + 1);
+                        next_ready = true;
+                        issue_s(0, j + 1);
+                    }
+                    if (j < nkv_b) issue_pv(1, j, cnt_b);
+                    tc_commit(kv_empty((kv_iter + j) & 1));  // every MMA reading this stage is issued
+                    if (j + 1 < nkv_b) {
+                        if (!next_ready) wait_kv(j + 1);
+                        issue_s(1, j + 1);
                     }
                 }
             }
             __syncwarp();
         } else {
-            // ---------------- softmax / epilogue: thread i owns row i ----------------
-            const int i = threadIdx.x;
-            const int t = min(t_first + (i >> log2g), t_last);
-            const bool live = t_first + (i >> log2g) <= t_last;
-            const int lim = C + t;  // last visible position
-            const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-            float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < nkv; ++j) {
-                const uint32_t it = kv_iter + j;
-                wait(s_full(it & 1), (it >> 1) & 1);
-                tc_fence_after();
-                const uint32_t scol = lane_base + ((it & 1) ? COL_S1 : COL_S0);
-                const int pos0 = j * ROWS;
-                // pass 1: row max of the scaled, masked scores (32 columns at a time)
-                float mx = -INFINITY;
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t sr[32];
-                    tmem_ld32(scol + 32 * q4, sr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (pos0 + 32 * q4 + c <= lim) mx = fmaxf(mx, __uint_as_float(sr[c]) * scale_log2);
-                }
-                const float m_new = fmaxf(m, mx);
-                if (j > 0) {
-                    wait(pv_done, (it - 1) & 1);  // PV(j-1) done: P buffer free, O settled
+            // ---------------- softmax / epilogue: thread i owns row i of tile x ----------------
+            const int x = warp >> 2;
+            const int nkv_x = x ? nkv_b : nkv_a;
+            const uint32_t cnt = x ? cnt_b : cnt_a;
+            if (nkv_x > 0) {
+                const int i = threadIdx.x - x * 128;
+                const int t_last = x ? tb_last : ta_last;
+                const int tt = t0 + x * TQ + (i >> log2g);
+                const bool live = tt <= t_last;
+                const int t = min(tt, t_last);
+                const int lim = C + t;  // last visible position
+                const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+                const uint32_t scol = lane_base + col_s(x), ocol = lane_base + col_o(x);
+                float m = -INFINITY, l = 0.f;
+                for (int j = 0; j < nkv_x; ++j) {
+                    wait(s_full(x), (cnt + j) & 1);
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, m_new > m + RESCALE_LOG2)) {
-                        const float alpha = ex2(m - m_new);
-                        l *= alpha;
-                        m = m_new;
+                    const int pos0 = j * ROWS;
+                    // pass 1: row max of the scaled, masked scores (32 columns at a time)
+                    float mx = -INFINITY;
 #pragma unroll 1
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t o[32];
-                            tmem_ld32(lane_base + COL_O + 32 * q4, o);
-                            tmem_wait_ld();
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t sr[32];
+                        tmem_ld32(scol + 32 * q4, sr);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                            tmem_st32(lane_base + COL_O + 32 * q4, o);
-                        }
-                        tmem_wait_st();
+                        for (int c = 0; c < 32; ++c)
+                            if (pos0 + 32 * q4 + c <= lim) mx = fmaxf(mx, __uint_as_float(sr[c]) * scale_log2);
                     }
-                } else {
-                    m = m_new;
-                }
-                // pass 2: P = 2^(s - m) as bf16 into row i of the P tile
+                    const float m_new = fmaxf(m, mx);
+                    if (j > 0) {
+                        wait(pv_done(x), (cnt + j - 1) & 1);  // PV(j-1) done: O settled
+                        tc_fence_after();
+                        if (__any_sync(0xffffffffu, m_new > m + RESCALE_LOG2)) {
+                            const float alpha = ex2(m - m_new);
+                            l *= alpha;
+                            m = m_new;
 #pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t sr[32];
-                    tmem_ld32(scol + 32 * q4, sr);
-                    tmem_wait_ld();
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                uint32_t o[32];
+                                tmem_ld32(ocol + 32 * q4, o);
+                                tmem_wait_ld();
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint32_t w[4];
+                                for (int c = 0; c < 32; ++c)
+                                    o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                                tmem_st32(ocol + 32 * q4, o);
+                            }
+                        }
+                    } else {
+                        m = m_new;
+                    }
+                    // pass 2: P = 2^(s - m) as bf16 into the first 64 columns of
+                    // this S row (chunk q4 of S -> P columns 16*q4 .. 16*q4+15, all
+                    // at or before S columns already read)
+#pragma unroll 1
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t sr[32];
+                        tmem_ld32(scol + 32 * q4, sr);
+                        tmem_wait_ld();
+                        uint32_t pw[16];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 8 * c8 + 2 * e;
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = 2 * e;
                             const int p = pos0 + 32 * q4 + c;
                             const float p0 = p <= lim ? ex2(__uint_as_float(sr[c]) * scale_log2 - m) : 0.f;
                             const float p1 = p + 1 <= lim ? ex2(__uint_as_float(sr[c + 1]) * scale_log2 - m) : 0.f;
                             l += p0 + p1;
-                            w[e] = pack_bf16x2(p0, p1);
+                            pw[e] = pack_bf16x2(p0, p1);
                         }
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(sP + sw128(i, 4 * q4 + c8)),
-                                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                     : "memory");
+                        tmem_st16(scol + 16 * q4, pw);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(p_full(x));
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(p_full);
-            }
-            // epilogue: O / l -> bf16
-            wait(pv_done, (kv_iter + nkv - 1) & 1);
-            tc_fence_after();
-            const float inv = 1.f / l;
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                 ((int64_t)(qoff + t) * Hq + g * G + (i & (G - 1))) * D;
+                // epilogue: O / l -> bf16
+                wait(pv_done(x), (cnt + nkv_x - 1) & 1);
+                tc_fence_after();
+                const float inv = 1.f / l;
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
+                                     ((int64_t)(qoff + t) * Hq + g * G + (i & (G - 1))) * D;
 #pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + COL_O + 32 * q4, o);
-                tmem_wait_ld();
-                if (live) {
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t o[32];
+                    tmem_ld32(ocol + 32 * q4, o);
+                    tmem_wait_ld();
+                    if (live) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + 32 * q4 + c) = v;
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
+                            v.y = pack_bf16x2(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                            v.z = pack_bf16x2(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+                            v.w = pack_bf16x2(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + 32 * q4 + c) = v;
+                        }
                     }
                 }
+                tc_fence_before();
             }
-            tc_fence_before();
         }
         kv_iter += nkv;
-        named_bar_sync(1, THREADS);  // item done: MMAs finished, O read, Q free
+        cnt_a += nkv_a;
+        cnt_b += nkv_b;
+        named_bar_sync(1, THREADS);  // item done: MMAs finished, O read, Q and TMEM free
         tc_fence_after();
     }
 
@@ -404,7 +439,7 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
     const int G = a.num_q_heads / a.num_kv_heads;
     int log2g = 0;
     while ((1 << log2g) < G) ++log2g;
-    const int TQ = ROWS >> log2g;
+    const int TQ2 = 2 * (ROWS >> log2g);
     const size_t smem = (size_t)OFF_PREFIX + (size_t)(a.batch + 1) * 4 + 1024;
     static std::mutex mu;
     static bool configured[64] = {false};
@@ -415,12 +450,15 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
         if (dev >= 0 && dev < 64 && !configured[dev]) {
             cudaError_t e = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  OFF_PREFIX + 4097 * 4 + 1024);
-            if (e != cudaSuccess) return e;
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return e;
+            }
             configured[dev] = true;
         }
     }
     // upper bound on work items: every request can add one partial block
-    const int64_t items = ((int64_t)a.total_q_tokens / TQ + a.batch) * a.num_kv_heads;
+    const int64_t items = ((int64_t)a.total_q_tokens / TQ2 + a.batch) * a.num_kv_heads;
     int64_t grid = device_sm_count();
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
