@@ -164,6 +164,7 @@ int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
  * cached_lens, extend_lens: device int32 [batch].
  * page_table: as for decode; pt_width columns per row.
  * out: device bf16 [total_q_tokens, num_q_heads, head_dim].
+ * sm_scale must be positive and finite (MINISGL_ERR_ARG otherwise).
  * Runs on the tensor cores (tcgen05, accumulators in tensor memory).
  * Supported: head_dim 128; num_q_heads/num_kv_heads in {1, 2, 4, 8, 16};
  * batch <= 4096.

@@ -3,6 +3,7 @@
 // Host-side argument checks, the thread-local error string, workspace
 // carving, and the launches.  No entry point allocates device memory or
 // synchronises with the device.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -216,6 +217,8 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
     if (G & (G - 1)) return fail(MINISGL_ERR_UNSUPPORTED, "extend_attn: group size %d not a power of 2", G);
     if (batch < 0 || batch > 4096) return fail(MINISGL_ERR_ARG, "extend_attn: batch %d outside [0, 4096]", batch);
     if (total_q_tokens < 0) return fail(MINISGL_ERR_ARG, "extend_attn: total_q_tokens < 0");
+    if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f))
+        return fail(MINISGL_ERR_ARG, "extend_attn: sm_scale must be positive and finite");
     if (batch == 0 || total_q_tokens == 0) return MINISGL_OK;
     if (!q || !page_table || !cached_lens || !extend_lens || !q_offsets || !out)
         return fail(MINISGL_ERR_ARG, "extend_attn: NULL pointer argument");

@@ -15,20 +15,21 @@
 //     The block is two query tiles A and B of 128 MMA rows each; a row is a
 //     (token, head) pair, so the G query heads that share KV head g ride in
 //     the same tile and every gathered K/V tile feeds 2*128 rows.
-//   * Producer warps 8-11 gather 128-token K and V tiles through page_table
+//   * Producer warps 8-9 gather 128-token K and V tiles through page_table
 //     with 16-byte cp.async into the 128-byte-swizzled layout the tensor core
 //     reads (K as a K-major B operand, V as an MN-major B operand), two
 //     stages deep; completion is tracked by mbarriers (cp.async.mbarrier.arrive).
-//   * Warp 12 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
+//   * Warp 10 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
 //     (M = N = 128) into tensor memory; O_X += P_X V with P_X read from
 //     tensor memory.  The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 //     keeps the tensor core on one tile while the other tile's softmax runs.
 //   * Softmax warpgroups 0 (warps 0-3, tile A) and 1 (warps 4-7, tile B):
 //     thread i owns TMEM lane (= MMA row) i of its tile.  It reads its S row
-//     (two passes of 32-column chunks: maximum, then exponentials), applies
-//     the causal limit C + t, keeps a running max m and sum l (base 2), and
-//     writes P = 2^(s - m) as bf16 back into the first 64 columns of its S
-//     row, where the PV MMA reads it.  O_X is rescaled in tensor memory only
+//     (64-column loads: maximum of the raw scores, then exponentials with
+//     packed f32x2 arithmetic), applies the causal limit C + t on diagonal
+//     tiles only, keeps a running max m and sum l (base 2), and writes
+//     P = 2^(s - m) as bf16 back into the upper 64 columns of its S row, where
+//     the PV MMA reads it.  O_X is rescaled in tensor memory only
 //     when the max has grown by more than 2^8 (the final O / l does not
 //     depend on when the rescale happens).  Epilogue: O / l -> bf16 -> global.
 //   * Tensor memory (512 columns): S_A 0-127, S_B 128-255, O_A 256-383,
@@ -58,9 +59,10 @@ constexpr int STAGES = 2;
 constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE_BYTES;  // 192 KB
 constexpr int OFF_TMEM_SLOT = OFF_BAR + 192;
 constexpr int OFF_PREFIX = OFF_BAR + 256;
-constexpr int THREADS = 416;              // 2 softmax warpgroups + 4 producer warps + 1 MMA warp
+constexpr int THREADS = 352;              // 2 softmax warpgroups + 2 producer warps + 1 MMA warp
 constexpr int PRODUCER_WARP0 = 8;
-constexpr int MMA_WARP = 12;
+constexpr int PRODUCER_THREADS = 64;
+constexpr int MMA_WARP = 10;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.f;
@@ -84,6 +86,72 @@ __device__ __forceinline__ void guarded_wait(uint32_t b, uint32_t parity, int *a
         *((volatile int *)abort_flag) = 1;
         atomicAdd(&g_kernel_timeouts, 1u);
     }
+}
+
+// ---- packed fp32 pairs (Blackwell f32x2 instructions) and 3-input max ----
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2split(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Max of the 64 raw scores in h whose column (0..63) is <= lim (all of them
+// when full).
+__device__ __forceinline__ float half_max(const uint32_t (&h)[64], bool full, int lim) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+    if (full) {
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+            m0 = fmax3(m0, __uint_as_float(h[c]), __uint_as_float(h[c + 1]));
+            m1 = fmax3(m1, __uint_as_float(h[c + 2]), __uint_as_float(h[c + 3]));
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (c <= lim) m0 = fmaxf(m0, __uint_as_float(h[c]));
+    }
+    return fmaxf(m0, m1);
+}
+
+// P = 2^(s*scale - m) for the 32 scores in q (0 past lim unless full), added
+// into the packed row sum l2 and stored as 16 bf16 pairs at TMEM column dst.
+__device__ __forceinline__ void quarter_softmax(const uint32_t (&q)[32], bool full, int lim,
+                                                uint64_t scale2, uint64_t negm2, uint64_t &l2,
+                                                uint32_t dst) {
+    uint32_t pw[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int c = 2 * e;
+        float s0 = __uint_as_float(q[c]), s1 = __uint_as_float(q[c + 1]);
+        if (!full) {
+            s0 = c <= lim ? s0 : -INFINITY;
+            s1 = c + 1 <= lim ? s1 : -INFINITY;
+        }
+        float x0, x1;
+        f2split(ffma2(f2(s0, s1), scale2, negm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        l2 = fadd2(l2, f2(p0, p1));
+        pw[e] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(dst, pw);
 }
 
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
@@ -120,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(kv_full(s), 128);
+            mbar_init(kv_full(s), PRODUCER_THREADS);
             mbar_init(kv_empty(s), 1);
         }
         for (int x = 0; x < 2; ++x) {
@@ -197,46 +265,32 @@ __global__ void __launch_bounds__(THREADS, 1)
 
         if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
             // ---------------- producer: Q_A, Q_B once, then K/V tiles ----------------
-            // Thread pt copies 16-byte chunk cc of rows tb*16 .. tb*16+15 of each
-            // 128-row tile (16 threads cover one 256-byte row).  The page-table
-            // entries of the next tile are fetched while this tile's copies go out.
+            // Thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31 of each
+            // 128-row tile (16 threads cover one 256-byte row).
+            constexpr int RPT = ROWS * 16 / PRODUCER_THREADS;  // rows per thread: 32
             const int pt = threadIdx.x - PRODUCER_WARP0 * 32;
             const int cc = pt & 15, tb = pt >> 4;
             const int32_t *ptab = a.page_table + (int64_t)r * a.pt_stride;
-            auto fetch_rows = [&](int j, int (&rows)[16]) {
-                const int p0 = j * ROWS + tb * 16;
-                if (p0 + 16 <= n_vis && ((reinterpret_cast<uintptr_t>(ptab + p0) & 15) == 0)) {
-                    const int4 *src = reinterpret_cast<const int4 *>(ptab + p0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int4 v = __ldg(src + q);
-                        rows[4 * q + 0] = v.x;
-                        rows[4 * q + 1] = v.y;
-                        rows[4 * q + 2] = v.z;
-                        rows[4 * q + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) rows[k] = p0 + k < n_vis ? __ldg(ptab + p0 + k) : -1;
-                }
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    rows[k] = rows[k] < 0 ? -1 : min(rows[k], a.num_rows - 1);
+            // each of the 16 threads sharing tb fetches 2 of its 32 rows; the
+            // rest come by shuffle within the half warp
+            auto fetch2 = [&](int j, int &ra, int &rb) {
+                const int p = j * ROWS + tb * RPT + 2 * cc;
+                ra = p < n_vis ? __ldg(ptab + p) : -1;
+                rb = p + 1 < n_vis ? __ldg(ptab + p + 1) : -1;
+                ra = ra < 0 ? -1 : min(ra, a.num_rows - 1);
+                rb = rb < 0 ? -1 : min(rb, a.num_rows - 1);
             };
-            int rows_cur[16], rows_nxt[16];
-            fetch_rows(0, rows_nxt);
+            int ra, rb;
+            fetch2(0, ra, rb);
             for (int j = 0; j < nkv; ++j) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) rows_cur[k] = rows_nxt[k];
-                if (j + 1 < nkv) fetch_rows(j + 1, rows_nxt);
                 const uint32_t it = kv_iter + j, st = it & 1;
                 if (it >= STAGES) wait(kv_empty(st), ((it >> 1) - 1) & 1);
                 if (j == 0) {
 #pragma unroll
                     for (int x = 0; x < 2; ++x)
 #pragma unroll 4
-                        for (int k = 0; k < 16; ++k) {
-                            const int i = tb * 16 + k;
+                        for (int k = 0; k < RPT; ++k) {
+                            const int i = tb * RPT + k;
                             const int t = t0 + x * TQ + (i >> log2g);
                             const bool live = t <= (x ? tb_last : ta_last) && (x == 0 || live_b);
                             const __nv_bfloat16 *src =
@@ -247,9 +301,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const uint32_t sK = sKV + st * 2 * TILE_BYTES, sV = sK + TILE_BYTES;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int tok = tb * 16 + k;
-                    const int row = rows_cur[k];
+                for (int k = 0; k < RPT; ++k) {
+                    const int tok = tb * RPT + k;
+                    const int row = __shfl_sync(0xffffffffu, (k & 1) ? rb : ra, (lane & 16) + (k >> 1));
                     const int64_t e = (int64_t)max(row, 0) * a.row_stride + (int64_t)g * D + cc * 8;
                     const int bytes = row >= 0 ? 16 : 0;
                     const uint32_t o = sw128(tok, cc);
@@ -257,6 +311,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     cp_async_16(sV + o, Vl + e, bytes);
                 }
                 cp_async_mbar_arrive_noinc(kv_full(st));
+                // next tile's rows: the loads are in flight while this thread
+                // waits for a free stage
+                if (j + 1 < nkv) fetch2(j + 1, ra, rb);
             }
             cp_async_wait<0>();
         } else if (warp == MMA_WARP) {
@@ -280,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < ROWS / 16; ++kk) {
                         const uint64_t bd = smem_desc_sw128(sV + kk * 2048, HALF, 1024);
-                        tc_mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bd, idesc_pv,
+                        tc_mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 64 + kk * 8, bd, idesc_pv,
                                        (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(pv_done(x));
@@ -324,29 +381,38 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int lim = C + t;  // last visible position
                 const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
                 const uint32_t scol = lane_base + col_s(x), ocol = lane_base + col_o(x);
-                float m = -INFINITY, l = 0.f;
+                float m = -INFINITY;            // running max of scaled scores (base 2)
+                uint64_t l2 = f2(0.f, 0.f);     // running row sum, two partial lanes
+                const uint64_t scale2 = f2(scale_log2, scale_log2);
                 for (int j = 0; j < nkv_x; ++j) {
                     wait(s_full(x), (cnt + j) & 1);
                     tc_fence_after();
-                    const int pos0 = j * ROWS;
-                    // pass 1: row max of the scaled, masked scores (32 columns at a time)
-                    float mx = -INFINITY;
-#pragma unroll 1
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t sr[32];
-                        tmem_ld32(scol + 32 * q4, sr);
+                    const int rel = lim - j * ROWS;  // last visible column of this tile
+                    const bool full = rel >= ROWS - 1;
+                    // pass 1: max of the raw scores (sm_scale > 0); the last 32
+                    // columns stay in registers for pass 2
+                    uint32_t top[32];
+                    float mx;
+                    {
+                        uint32_t h[64];
+                        tmem_ld64(scol, h);
                         tmem_wait_ld();
+                        mx = half_max(h, full, rel);
+                        tmem_ld64(scol + 64, h);
+                        tmem_wait_ld();
+                        mx = fmaxf(mx, half_max(h, full, rel - 64));
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (pos0 + 32 * q4 + c <= lim) mx = fmaxf(mx, __uint_as_float(sr[c]) * scale_log2);
+                        for (int c = 0; c < 32; ++c) top[c] = h[32 + c];
                     }
-                    const float m_new = fmaxf(m, mx);
+                    const float m_new = fmaxf(m, mx * scale_log2);
                     if (j > 0) {
                         wait(pv_done(x), (cnt + j - 1) & 1);  // PV(j-1) done: O settled
                         tc_fence_after();
                         if (__any_sync(0xffffffffu, m_new > m + RESCALE_LOG2)) {
                             const float alpha = ex2(m - m_new);
-                            l *= alpha;
+                            float la, lb;
+                            f2split(l2, la, lb);
+                            l2 = f2(la * alpha, lb * alpha);
                             m = m_new;
 #pragma unroll 1
                             for (int q4 = 0; q4 < 4; ++q4) {
@@ -362,30 +428,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                     } else {
                         m = m_new;
                     }
-                    // pass 2: P = 2^(s - m) as bf16 into the first 64 columns of
-                    // this S row (chunk q4 of S -> P columns 16*q4 .. 16*q4+15, all
-                    // at or before S columns already read)
+                    // pass 2: P as bf16 into the upper 64 columns of this S row,
+                    // quarter by quarter from the top: S columns 32q..32q+31 ->
+                    // P columns 64+16q..64+16q+15, which only ever overwrites S
+                    // columns already consumed
+                    const uint64_t negm2 = f2(-m, -m);
+                    quarter_softmax(top, full, rel - 96, scale2, negm2, l2, scol + 112);
 #pragma unroll 1
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t sr[32];
-                        tmem_ld32(scol + 32 * q4, sr);
+                    for (int q4 = 2; q4 >= 0; --q4) {
+                        uint32_t qv[32];
+                        tmem_ld32(scol + 32 * q4, qv);
                         tmem_wait_ld();
-                        uint32_t pw[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int c = 2 * e;
-                            const int p = pos0 + 32 * q4 + c;
-                            const float p0 = p <= lim ? ex2(__uint_as_float(sr[c]) * scale_log2 - m) : 0.f;
-                            const float p1 = p + 1 <= lim ? ex2(__uint_as_float(sr[c + 1]) * scale_log2 - m) : 0.f;
-                            l += p0 + p1;
-                            pw[e] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16(scol + 16 * q4, pw);
+                        quarter_softmax(qv, full, rel - 32 * q4, scale2, negm2, l2, scol + 64 + 16 * q4);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(p_full(x));
                 }
+                float la, lb;
+                f2split(l2, la, lb);
+                const float l = la + lb;
                 // epilogue: O / l -> bf16
                 wait(pv_done(x), (cnt + nkv_x - 1) & 1);
                 tc_fence_after();

@@ -86,6 +86,11 @@ def test_error_codes_on_host(lib):
     d3.row_stride = 2 * 128
     assert lib.minisgl_extend_attn(ref(d3), 0, fake, 6, fake, 2, 32, 32, fake, fake, fake, 10,
                                    0.1, fake, None) == -4
+    # extend needs a positive, finite sm_scale
+    assert lib.minisgl_extend_attn(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
+                                   -0.1, fake, None) == -1
+    assert lib.minisgl_extend_attn(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
+                                   float("nan"), fake, None) == -1
     # empty work is a no-op that touches nothing
     assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 1024, 1024, fake, 0, None) == 0
     assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 0, 32, 32, fake, 0.1, fake, fake,
