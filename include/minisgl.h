@@ -23,8 +23,15 @@
  *
  * Conventions for every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller; the
- *     library never allocates, frees or keeps device memory, and keeps no
- *     state between calls besides a thread-local error string.
+ *     library never allocates or frees device memory at run time.  Besides a
+ *     thread-local error string it keeps only two things in its own,
+ *     statically sized device memory: the 32 MiB scratch array of
+ *     minisgl_decode_attn_noalloc, and 64 work-ticket counters that
+ *     minisgl_extend_attn uses to hand out work items to its thread blocks
+ *     (each call draws one of the 64 in turn and leaves it at zero when its
+ *     kernel completes, so more than 64 extend calls in flight at the same
+ *     time on unordered streams would share counters and give wrong
+ *     results).
  *   - Element type is bf16 for K, V, Q and the output (MINISGL_BF16); index
  *     tensors are int32.  Strides are in elements.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default

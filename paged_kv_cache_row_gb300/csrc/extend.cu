@@ -38,6 +38,7 @@
 //   * Every mbarrier wait is bounded in time; a wait that runs out sets a
 //     flag, the kernel finishes without further waiting (its output is then
 //     garbage) and a device counter of such events is increased.
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -46,6 +47,14 @@
 namespace minisgl {
 
 __device__ unsigned int g_kernel_timeouts = 0;
+
+// Work tickets for the extend kernel's dynamic item schedule: per call slot,
+// the next ticket and the number of CTAs that have finished.  The last CTA
+// of a launch puts both back to zero.
+struct SchedSlot {
+    unsigned int next, done;
+};
+__device__ SchedSlot g_sched[64];
 
 namespace {
 
@@ -58,7 +67,10 @@ constexpr int OFF_KV = 2 * TILE_BYTES;    // stage s: K at +2s*TILE, V at +(2s+1
 constexpr int STAGES = 2;
 constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE_BYTES;  // 192 KB
 constexpr int OFF_TMEM_SLOT = OFF_BAR + 192;
-constexpr int OFF_PREFIX = OFF_BAR + 256;
+constexpr int OFF_RING = OFF_BAR + 256;   // ring of RING work-item descriptors (64 B each)
+constexpr int RING = 8;
+constexpr int OFF_PREFIX = OFF_RING + RING * 64;
+constexpr int SCHED_SLOTS = 64;           // per-call work-ticket counters
 constexpr int THREADS = 352;              // 2 softmax warpgroups + 2 producer warps + 1 MMA warp
 constexpr int PRODUCER_WARP0 = 8;
 constexpr int PRODUCER_THREADS = 64;
@@ -158,10 +170,48 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
+// One work item: request r, KV head g, query tiles A (new tokens t0 ..
+// ta_last) and B (t0 + TQ .. tb_last, when live_b), C cached tokens before
+// them; nkv_a / nkv_b KV tiles seen by each tile.
+struct Item {
+    int r, g, t0, ta_last, tb_last, C, qoff, nkv_a, nkv_b;
+    bool live_b;
+    __device__ __forceinline__ int nkv() const { return max(nkv_a, nkv_b); }
+    __device__ __forceinline__ int n_vis() const { return C + tb_last + 1; }  // KV positions seen
+};
+
+// Work item `item` from the per-request prefix of item counts in shared
+// memory (binary search) and the request's lengths from global memory.
+__device__ __forceinline__ Item load_item(const ExtendArgs &a, const int32_t *s_prefix, int item,
+                                          int TQ) {
+    int lo = 0, hi = a.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_prefix[mid] <= item) lo = mid; else hi = mid;
+    }
+    Item it;
+    it.r = lo;
+    const int nqb = (s_prefix[lo + 1] - s_prefix[lo]) / a.num_kv_heads;
+    const int off = item - s_prefix[lo];
+    it.g = off / nqb;
+    const int qb = off - it.g * nqb;
+    const int W = a.pt_width;
+    it.C = min(max(__ldg(a.cached_lens + lo), 0), W);
+    const int E = min(max(__ldg(a.extend_lens + lo), 0), W - it.C);
+    it.qoff = __ldg(a.q_offsets + lo);
+    it.t0 = qb * 2 * TQ;
+    it.ta_last = min(it.t0 + TQ, E) - 1;
+    it.live_b = it.t0 + TQ < E;
+    it.tb_last = it.live_b ? min(it.t0 + 2 * TQ, E) - 1 : it.ta_last;
+    it.nkv_a = (it.C + it.ta_last + 1 + ROWS - 1) / ROWS;
+    it.nkv_b = it.live_b ? (it.C + it.tb_last + 1 + ROWS - 1) / ROWS : 0;
+    return it;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(THREADS, 1)
-    extend_kernel(const ExtendArgs a, const float scale_log2, const int log2g) {
+    extend_kernel(const ExtendArgs a, const float scale_log2, const int log2g, const int slot) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,7 +224,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto s_full = [&](int x) { return bar + 32 + 8 * x; };
     auto p_full = [&](int x) { return bar + 48 + 8 * x; };
     auto pv_done = [&](int x) { return bar + 64 + 8 * x; };
-    const uint32_t fin = bar + 80;
+    const uint32_t fin = bar + 80, q_empty = bar + 88;
+    auto item_ready = [&](uint32_t n) { return bar + 96 + 8 * (n % RING); };
+    auto ring = [&](uint32_t n) { return reinterpret_cast<Item *>(base + OFF_RING + 64 * (n % RING)); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + OFF_TMEM_SLOT);
     int32_t *s_prefix = reinterpret_cast<int32_t *>(base + OFF_PREFIX);
 
@@ -197,6 +249,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(pv_done(x), 1);
         }
         mbar_init(fin, 1);
+        mbar_init(q_empty, 1);
+        for (int k = 0; k < RING; ++k) mbar_init(item_ready(k), 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -239,38 +293,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t idesc_qk = idesc_bf16_f32(ROWS, ROWS, false);
     const uint32_t idesc_pv = idesc_bf16_f32(ROWS, D, true);
 
-    // Running counts shared by all roles: KV tiles, and tiles processed per query tile.
-    uint32_t kv_iter = 0, cnt_a = 0, cnt_b = 0;
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        int lo = 0, hi = B;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_prefix[mid] <= item) lo = mid; else hi = mid;
-        }
-        const int r = lo;
-        const int nqb = (s_prefix[r + 1] - s_prefix[r]) / Hkv;
-        const int off = item - s_prefix[r];
-        const int g = off / nqb, qb = off - g * nqb;
-        const int C = min(max(__ldg(a.cached_lens + r), 0), W);
-        const int E = min(max(__ldg(a.extend_lens + r), 0), W - C);
-        const int qoff = __ldg(a.q_offsets + r);
-        const int t0 = qb * TQ2;                    // first new token of tile A
-        const int ta_last = min(t0 + TQ, E) - 1;    // last live token of tile A
-        const bool live_b = t0 + TQ < E;
-        const int tb_last = live_b ? min(t0 + TQ2, E) - 1 : ta_last;
-        const int nkv_a = (C + ta_last + 1 + ROWS - 1) / ROWS;
-        const int nkv_b = live_b ? (C + tb_last + 1 + ROWS - 1) / ROWS : 0;
-        const int nkv = max(nkv_a, nkv_b);
-        const int n_vis = C + tb_last + 1;         // KV positions the item can see
-
-        if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
-            // ---------------- producer: Q_A, Q_B once, then K/V tiles ----------------
-            // Thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31 of each
-            // 128-row tile (16 threads cover one 256-byte row).
-            constexpr int RPT = ROWS * 16 / PRODUCER_THREADS;  // rows per thread: 32
-            const int pt = threadIdx.x - PRODUCER_WARP0 * 32;
-            const int cc = pt & 15, tb = pt >> 4;
-            const int32_t *ptab = a.page_table + (int64_t)r * a.pt_stride;
+    // Schedule: the CTA's first item is blockIdx.x, later ones come from a
+    // ticket counter shared by the launch (items gridDim.x, gridDim.x + 1, ...
+    // in the order CTAs ask), so CTAs that drew short items take more.  The
+    // producers, which run ahead, draw the tickets (one item early) and
+    // publish each item's description in a ring of RING slots, slot n for
+    // the CTA's n-th item, with an mbarrier per slot; a description with
+    // r = -1 ends the CTA's work.  A slot is rewritten RING items later, long
+    // after the other roles have read it: the producers cannot get more than
+    // two items ahead of the MMA warp (they wait for its q_empty), nor the MMA
+    // warp more than one ahead of the softmax warps (it waits for their P).
+    // The roles run through the items without a CTA-wide barrier in between;
+    // each keeps its own running counts of KV tiles and of tiles per query
+    // tile.
+    SchedSlot *sched = &g_sched[slot];
+    if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
+        // ---------------- producer: Q_A, Q_B per item, then K/V tiles ----------------
+        // Thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31 of each
+        // 128-row tile (16 threads cover one 256-byte row).  An item's Q goes
+        // out with its first K/V tile, once the MMA warp has released the Q
+        // buffers (the previous item's last S is done).
+        constexpr int RPT = ROWS * 16 / PRODUCER_THREADS;  // rows per thread: 32
+        const int pt = threadIdx.x - PRODUCER_WARP0 * 32;
+        const int cc = pt & 15, tb = pt >> 4;
+        uint32_t kv_iter = 0, n_items = 0;
+        int item = blockIdx.x;  // this CTA's n-th item (thread 0's copy)
+        for (;; ++n_items) {
+            if (pt == 0) {
+                Item it;
+                it.r = -1;
+                if (item < total_items && !*((volatile int *)&s_abort)) it = load_item(a, s_prefix, item, TQ);
+                // next ticket, drawn one item early
+                if (it.r >= 0) item = (int)gridDim.x + (int)atomicAdd(&sched->next, 1u);
+                *ring(n_items) = it;
+                mbar_arrive(item_ready(n_items));
+            }
+            named_bar_sync(2, PRODUCER_THREADS);
+            const Item cur = *ring(n_items);
+            if (cur.r < 0) break;
+            const int32_t *ptab = a.page_table + (int64_t)cur.r * a.pt_stride;
+            const int n_vis = cur.n_vis(), nkv = cur.nkv();
             // each of the 16 threads sharing tb fetches 2 of its 32 rows; the
             // rest come by shuffle within the half warp
             auto fetch2 = [&](int j, int &ra, int &rb) {
@@ -286,15 +348,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t it = kv_iter + j, st = it & 1;
                 if (it >= STAGES) wait(kv_empty(st), ((it >> 1) - 1) & 1);
                 if (j == 0) {
+                    if (n_items > 0) wait(q_empty, (n_items - 1) & 1);
 #pragma unroll
                     for (int x = 0; x < 2; ++x)
 #pragma unroll 4
                         for (int k = 0; k < RPT; ++k) {
                             const int i = tb * RPT + k;
-                            const int t = t0 + x * TQ + (i >> log2g);
-                            const bool live = t <= (x ? tb_last : ta_last) && (x == 0 || live_b);
+                            const int t = cur.t0 + x * TQ + (i >> log2g);
+                            const bool live = t <= (x ? cur.tb_last : cur.ta_last) && (x == 0 || cur.live_b);
                             const __nv_bfloat16 *src =
-                                live ? Q + ((int64_t)(qoff + t) * Hq + g * G + (i & (G - 1))) * D + cc * 8
+                                live ? Q + ((int64_t)(cur.qoff + t) * Hq + cur.g * G + (i & (G - 1))) * D + cc * 8
                                      : Q;
                             cp_async_16(sQ + x * TILE_BYTES + sw128(i, cc), src, live ? 16 : 0);
                         }
@@ -304,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int k = 0; k < RPT; ++k) {
                     const int tok = tb * RPT + k;
                     const int row = __shfl_sync(0xffffffffu, (k & 1) ? rb : ra, (lane & 16) + (k >> 1));
-                    const int64_t e = (int64_t)max(row, 0) * a.row_stride + (int64_t)g * D + cc * 8;
+                    const int64_t e = (int64_t)max(row, 0) * a.row_stride + (int64_t)cur.g * D + cc * 8;
                     const int bytes = row >= 0 ? 16 : 0;
                     const uint32_t o = sw128(tok, cc);
                     cp_async_16(sK + o, Kl + e, bytes);
@@ -315,10 +378,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // waits for a free stage
                 if (j + 1 < nkv) fetch2(j + 1, ra, rb);
             }
-            cp_async_wait<0>();
-        } else if (warp == MMA_WARP) {
-            // ---------------- MMA issuer ----------------
-            if (lane == 0) {
+            kv_iter += nkv;
+        }
+        cp_async_wait<0>();
+    } else if (warp == MMA_WARP) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t kv_iter = 0, cnt_a = 0, cnt_b = 0;
+            for (uint32_t n = 0;; ++n) {
+                wait(item_ready(n), (n / RING) & 1);
+                if (*((volatile int *)&s_abort)) break;
+                const Item cur = *ring(n);
+                if (cur.r < 0) break;
+                const int nkv_a = cur.nkv_a, nkv_b = cur.nkv_b, nkv = cur.nkv();
                 auto issue_s = [&](int x, int j) {  // S_X(j) = Q_X K(j)^T
                     const uint32_t sK = sKV + ((kv_iter + j) & 1) * 2 * TILE_BYTES;
                     const uint32_t qx = sQ + x * TILE_BYTES;
@@ -347,9 +419,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     fence_proxy_async_smem();
                     tc_fence_after();
                 };
+                // The first S of each tile of this item reads Q_A / Q_B; once the
+                // last of them is issued, q_empty (fired when they are done)
+                // lets the producers bring in the next item's Q.
                 wait_kv(0);
                 issue_s(0, 0);
                 if (nkv_b > 0) issue_s(1, 0);
+                if (nkv == 1) tc_commit(q_empty);
                 for (int j = 0; j < nkv; ++j) {
                     bool next_ready = false;
                     if (j < nkv_a) issue_pv(0, j, cnt_a);
@@ -364,26 +440,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (!next_ready) wait_kv(j + 1);
                         issue_s(1, j + 1);
                     }
+                    if (j + 2 == nkv) tc_commit(q_empty);
                 }
+                kv_iter += nkv;
+                cnt_a += nkv_a;
+                cnt_b += nkv_b;
             }
-            __syncwarp();
-        } else {
-            // ---------------- softmax / epilogue: thread i owns row i of tile x ----------------
-            const int x = warp >> 2;
-            const int nkv_x = x ? nkv_b : nkv_a;
-            const uint32_t cnt = x ? cnt_b : cnt_a;
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax / epilogue: thread i owns row i of tile x ----------------
+        // O_X is read out before this warpgroup publishes the next item's
+        // first P_X, and the MMA that overwrites O_X (that item's first PV_X)
+        // waits for that P_X.
+        const int x = warp >> 2;
+        const int i = threadIdx.x - x * 128;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t scol = lane_base + col_s(x), ocol = lane_base + col_o(x);
+        const uint64_t scale2 = f2(scale_log2, scale_log2);
+        uint32_t cnt = 0;  // tiles of query tile x processed
+        for (uint32_t n = 0;; ++n) {
+            wait(item_ready(n), (n / RING) & 1);
+            if (*((volatile int *)&s_abort)) break;
+            const Item cur = *ring(n);
+            if (cur.r < 0) break;
+            const int nkv_x = x ? cur.nkv_b : cur.nkv_a;
             if (nkv_x > 0) {
-                const int i = threadIdx.x - x * 128;
-                const int t_last = x ? tb_last : ta_last;
-                const int tt = t0 + x * TQ + (i >> log2g);
+                const int t_last = x ? cur.tb_last : cur.ta_last;
+                const int tt = cur.t0 + x * TQ + (i >> log2g);
                 const bool live = tt <= t_last;
                 const int t = min(tt, t_last);
-                const int lim = C + t;  // last visible position
-                const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-                const uint32_t scol = lane_base + col_s(x), ocol = lane_base + col_o(x);
+                const int lim = cur.C + t;  // last visible position
                 float m = -INFINITY;            // running max of scaled scores (base 2)
                 uint64_t l2 = f2(0.f, 0.f);     // running row sum, two partial lanes
-                const uint64_t scale2 = f2(scale_log2, scale_log2);
                 for (int j = 0; j < nkv_x; ++j) {
                     wait(s_full(x), (cnt + j) & 1);
                     tc_fence_after();
@@ -453,7 +542,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const float inv = 1.f / l;
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                     ((int64_t)(qoff + t) * Hq + g * G + (i & (G - 1))) * D;
+                                     ((int64_t)(cur.qoff + t) * Hq + cur.g * G + (i & (G - 1))) * D;
 #pragma unroll 1
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t o[32];
@@ -472,13 +561,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 tc_fence_before();
+                cnt += nkv_x;
             }
         }
-        kv_iter += nkv;
-        cnt_a += nkv_a;
-        cnt_b += nkv_b;
-        named_bar_sync(1, THREADS);  // item done: MMAs finished, O read, Q and TMEM free
-        tc_fence_after();
     }
 
 #undef wait
@@ -494,6 +579,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+    // the last CTA to finish leaves the ticket counter at zero for the next
+    // launch that uses this slot (a launch in the same stream starts drawing
+    // only after this grid has completed)
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&sched->done, 1u) == gridDim.x - 1) {
+            sched->next = 0;
+            sched->done = 0;
+            __threadfence();
+        }
+    }
 }
 
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
@@ -524,8 +620,12 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
     int64_t grid = device_sm_count();
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
+    // a ticket counter slot per call, so calls running at the same time on
+    // different streams do not share one
+    static std::atomic<unsigned> next_slot{0};
+    const int slot = (int)(next_slot.fetch_add(1u) % SCHED_SLOTS);
     return launch_pdl(extend_kernel, dim3((unsigned)grid), dim3(THREADS), smem, s, a,
-                      a.sm_scale * LOG2E, log2g);
+                      a.sm_scale * LOG2E, log2g, slot);
 }
 
 cudaError_t read_kernel_timeouts(unsigned int *count) {
