@@ -19,7 +19,7 @@
 //     with 16-byte cp.async into the 128-byte-swizzled layout the tensor core
 //     reads (K as a K-major B operand, V as an MN-major B operand), two
 //     stages deep; completion is tracked by mbarriers (cp.async.mbarrier.arrive).
-//   * Warp 10 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
+//   * Warp 11 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
 //     (M = N = 128) into tensor memory; O_X += P_X V with P_X read from
 //     tensor memory.  The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 //     keeps the tensor core on one tile while the other tile's softmax runs.
@@ -71,10 +71,14 @@ constexpr int OFF_RING = OFF_BAR + 256;   // ring of RING work-item descriptors 
 constexpr int RING = 8;
 constexpr int OFF_PREFIX = OFF_RING + RING * 64;
 constexpr int SCHED_SLOTS = 64;           // per-call work-ticket counters
-constexpr int THREADS = 352;              // 2 softmax warpgroups + 2 producer warps + 1 MMA warp
+constexpr int THREADS = 384;              // 2 softmax warpgroups, 2 producer warps, idle warp, MMA warp
 constexpr int PRODUCER_WARP0 = 8;
 constexpr int PRODUCER_THREADS = 64;
-constexpr int MMA_WARP = 10;
+constexpr int PRODUCER_WARPS = 2;
+// The MMA issuer is warp 11: warps are spread over the four schedulers by
+// warp index mod 4, and scheduler 3 carries only softmax warps 3 and 7
+// besides it (warp 10, on scheduler 2 with softmax warps 2 and 6, idles).
+constexpr int MMA_WARP = 11;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.f;
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // each keeps its own running counts of KV tiles and of tiles per query
     // tile.
     SchedSlot *sched = &g_sched[slot];
-    if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
+    if (warp >= PRODUCER_WARP0 && warp < PRODUCER_WARP0 + PRODUCER_WARPS) {
         // ---------------- producer: Q_A, Q_B per item, then K/V tiles ----------------
         // Thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31 of each
         // 128-row tile (16 threads cover one 256-byte row).  An item's Q goes
@@ -383,7 +387,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         cp_async_wait<0>();
     } else if (warp == MMA_WARP) {
         // ---------------- MMA issuer ----------------
+        // One thread issues every MMA, and the tensor core accepts only a
+        // couple of MMAs ahead, so whatever this thread executes between two
+        // MMA groups leaves the tensor core idle.  Hence: the shared-memory
+        // descriptors are built once here, and the one for K-slice kk of a
+        // tile is its tile's descriptor plus a constant (the 14-bit address
+        // field holds addr >> 4, below 2^14 for any shared-memory address, so
+        // the sum never carries into the next field); and a wait first probes
+        // the barrier once, taking the bounded, abort-aware path only when
+        // the phase is not complete yet.
         if (lane == 0) {
+            const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t dq1 = smem_desc_sw128(sQ + TILE_BYTES, 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(sKV, 16, 1024);
+            const uint64_t dk1 = smem_desc_sw128(sKV + 2 * TILE_BYTES, 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(sKV + TILE_BYTES, HALF, 1024);
+            const uint64_t dv1 = smem_desc_sw128(sKV + 3 * TILE_BYTES, HALF, 1024);
+            auto mwait = [&](uint32_t b, uint32_t par) {
+                if (!mbar_try_wait(b, par)) wait(b, par);
+            };
             uint32_t kv_iter = 0, cnt_a = 0, cnt_b = 0;
             for (uint32_t n = 0;; ++n) {
                 wait(item_ready(n), (n / RING) & 1);
@@ -392,30 +414,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (cur.r < 0) break;
                 const int nkv_a = cur.nkv_a, nkv_b = cur.nkv_b, nkv = cur.nkv();
                 auto issue_s = [&](int x, int j) {  // S_X(j) = Q_X K(j)^T
-                    const uint32_t sK = sKV + ((kv_iter + j) & 1) * 2 * TILE_BYTES;
-                    const uint32_t qx = sQ + x * TILE_BYTES;
+                    const uint64_t dk = ((kv_iter + j) & 1) ? dk1 : dk0;
+                    const uint64_t dq = x ? dq1 : dq0;
+                    const uint32_t ds = tmem + col_s(x);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(qx + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(sK + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-                        tc_mma_bf16(tmem + col_s(x), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                        // K-slice kk of a K-major 128-byte-swizzled tile: 64-column
+                        // region kk / 4, 32-byte step kk % 4 within the row
+                        const uint64_t off = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+                        tc_mma_bf16(ds, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(s_full(x));
                 };
                 auto issue_pv = [&](int x, int j, uint32_t cnt) {  // O_X += P_X(j) V(j)
-                    wait(p_full(x), (cnt + j) & 1);
+                    mwait(p_full(x), (cnt + j) & 1);
                     tc_fence_after();
-                    const uint32_t sV = sKV + ((kv_iter + j) & 1) * 2 * TILE_BYTES + TILE_BYTES;
+                    const uint64_t dv = ((kv_iter + j) & 1) ? dv1 : dv0;
+                    const uint32_t dO = tmem + col_o(x), dP = tmem + col_s(x) + 64;
 #pragma unroll
-                    for (int kk = 0; kk < ROWS / 16; ++kk) {
-                        const uint64_t bd = smem_desc_sw128(sV + kk * 2048, HALF, 1024);
-                        tc_mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 64 + kk * 8, bd, idesc_pv,
+                    for (int kk = 0; kk < ROWS / 16; ++kk)  // 16 tokens (2 KB of V) per MMA
+                        tc_mma_bf16_ts(dO, dP + kk * 8, dv + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                                        (j > 0 || kk > 0) ? 1u : 0u);
-                    }
                     tc_commit(pv_done(x));
                 };
                 auto wait_kv = [&](int j) {
-                    wait(kv_full((kv_iter + j) & 1), ((kv_iter + j) >> 1) & 1);
+                    mwait(kv_full((kv_iter + j) & 1), ((kv_iter + j) >> 1) & 1);
                     fence_proxy_async_smem();
                     tc_fence_after();
                 };
@@ -448,7 +471,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 8) {
         // ---------------- softmax / epilogue: thread i owns row i of tile x ----------------
         // O_X is read out before this warpgroup publishes the next item's
         // first P_X, and the MMA that overwrites O_X (that item's first PV_X)
