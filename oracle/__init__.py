@@ -81,6 +81,8 @@ class Oracle:
         self.lib.oracle_extend.restype = ctypes.c_int
         self.lib.oracle_lse_merge.argtypes = [i64, i64, i32, vp, vp, vp, vp]
         self.lib.oracle_lse_merge.restype = None
+        self.lib.oracle_rope.argtypes = [vp, i64, i32, i32, vp, vp, i64, vp]
+        self.lib.oracle_rope.restype = ctypes.c_int
 
     # -- store_kv ---------------------------------------------------------
     def store_kv(self, k_pool: np.ndarray, v_pool: np.ndarray, k, v, out_loc) -> None:
@@ -142,6 +144,28 @@ class Oracle:
         lse = np.zeros(vec_shape, dtype=np.float64)
         self.lib.oracle_lse_merge(S, n_vec, d, _p(o_parts), _p(lse_parts), _p(out), _p(lse))
         return out, lse
+
+    # -- rope -------------------------------------------------------------
+    def rope(self, x, positions, cos_sin_cache):
+        """x [N, H, d] bf16 / uint16; positions [N] int32; cos_sin_cache
+        [max_positions, d] float32 ([cos | sin] per row).  Returns the rotated
+        x as float64 [N, H, d]."""
+        xs = _u16(x)
+        pos = _i32(positions)
+        try:
+            import torch
+            if isinstance(cos_sin_cache, torch.Tensor):
+                cos_sin_cache = cos_sin_cache.detach().cpu().numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        cache = np.ascontiguousarray(cos_sin_cache, dtype=np.float32)
+        N, H, d = xs.shape
+        assert cache.shape[1] == d and pos.shape[0] == N
+        out = np.zeros((N, H, d), dtype=np.float64)
+        rc = self.lib.oracle_rope(_p(xs), N, H, d, _p(pos), _p(cache), cache.shape[0], _p(out))
+        if rc != 0:
+            raise ValueError("oracle_rope: position outside the cache or odd head_dim")
+        return out
 
 
 _default: Optional[Oracle] = None

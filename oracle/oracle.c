@@ -28,6 +28,8 @@
  *     backends passage); used here only as a definition to check against.
  *   - GQA: query head h reads KV head h / (H_q / H_kv) (contiguous groups;
  *     the pages name GQA but give no mapping, so this is the plain reading).
+ *   - rope: rotary position embedding of q and k by a cached cos/sin table
+ *     (deep dive, section 7.3), the step just before store_kv in each layer.
  *
  * Numbers: inputs are bf16 bit patterns, widened exactly to double; all
  * arithmetic is double; outputs are double.  A NaN anywhere in a gathered row
@@ -251,4 +253,46 @@ void oracle_lse_merge(int64_t n_parts, int64_t n_vec, int32_t head_dim, const do
         if (lse_out)
             lse_out[i] = top + log(total);
     }
+}
+
+/* ---------------------------------------------------------------------- */
+/* rotary position embedding (RoPE)                                        */
+/* ---------------------------------------------------------------------- */
+/* "mini-sglang architecture deep dive", section 7.3 (RoPE): a cache holds,
+ * for every position p, the row [cos(p*f_0) .. cos(p*f_{d/2-1}),
+ * sin(p*f_0) .. sin(p*f_{d/2-1})] in float32, with f_i = base^(-2i/d) and
+ * rotary_dim = head_size = d; the library call it makes rotates q and k in
+ * place by the cached angles of each token's position.  The pages do not say
+ * which elements form a rotated pair; this follows the half-split pairing
+ * (element i with element i + d/2), the default of the routine the page
+ * calls:
+ *     y[i]       = x[i] * cos_i - x[i + d/2] * sin_i
+ *     y[i + d/2] = x[i + d/2] * cos_i + x[i] * sin_i,      i < d/2.
+ * x: [n_tokens, num_heads, head_dim] bf16 bits (token stride
+ * num_heads*head_dim); cos_sin_cache: [max_positions, head_dim] float32;
+ * out: [n_tokens, num_heads, head_dim] double.  Returns -1 if a position lies
+ * outside [0, max_positions) or head_dim is odd. */
+int oracle_rope(const uint16_t *x, int64_t n_tokens, int32_t num_heads, int32_t head_dim,
+                const int32_t *positions, const float *cos_sin_cache, int64_t max_positions,
+                double *out)
+{
+    if (head_dim % 2 != 0)
+        return -1;
+    const int32_t half = head_dim / 2;
+    for (int64_t i = 0; i < n_tokens; i++) {
+        const int64_t pos = positions[i];
+        if (pos < 0 || pos >= max_positions)
+            return -1;
+        const float *cs = cos_sin_cache + pos * head_dim;
+        for (int32_t h = 0; h < num_heads; h++) {
+            const int64_t at = (i * num_heads + h) * (int64_t)head_dim;
+            for (int32_t j = 0; j < half; j++) {
+                const double c = (double)cs[j], s = (double)cs[half + j];
+                const double x1 = widen(x[at + j]), x2 = widen(x[at + half + j]);
+                out[at + j] = x1 * c - x2 * s;
+                out[at + half + j] = x2 * c + x1 * s;
+            }
+        }
+    }
+    return 0;
 }

@@ -10,7 +10,10 @@ the oracle disagrees with:
     table with 64-row pages reads the same values as one with single rows;
     requests sharing radix-cache prefix rows equal requests with private
     copies; CUDA-Graph padding requests touch only the dummy row);
-  * values printed in the golden fixtures under tests/golden/.
+  * values printed in the golden fixtures under tests/golden/;
+  * for RoPE: position 0 is the identity, the rotation equals complex
+    multiplication by exp(1j*theta) (numpy), and scores depend only on the
+    relative position.
 They are kept apart from the test functions so tests/test_oracle_mutations.py
 can run the same pins against deliberately broken copies of the oracle and
 check that every planted mistake is caught.
@@ -407,6 +410,71 @@ def pin_golden_page_table_example(orc):
     assert np.abs(lse[:, 0] - exp_l).max() <= 1e-12, "golden page-table example: lse"
 
 
+# --------------------------------------------------------------------------- #
+# rotary position embedding (deep dive, section 7.3)
+# --------------------------------------------------------------------------- #
+def _angles(d, positions, base=10000.0):
+    """theta[p, i] = p * base^(-2i/d) in float64 (the pages' frequencies)."""
+    inv = base ** (-np.arange(0, d, 2, dtype=np.float64) / d)
+    return np.outer(np.asarray(positions, dtype=np.float64), inv)
+
+
+def _cos_sin_table(d, max_pos, base=10000.0):
+    """[cos | sin] rows per position, float32 as the pages store them."""
+    ang = _angles(d, np.arange(max_pos), base)
+    return np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32)
+
+
+def pin_rope_position_zero_is_identity(orc):
+    g = torch.Generator().manual_seed(31)
+    x = rnd((5, 3, 16), g)
+    out = orc.rope(x, np.zeros(5, dtype=np.int32), _cos_sin_table(16, 8))
+    assert np.array_equal(out, f64(x).numpy()), "position 0 must leave x unchanged"
+
+
+def pin_rope_is_complex_rotation(orc):
+    """RoPE multiplies z_i = x_i + 1j*x_{i+d/2} by exp(1j*theta_i); the
+    reference uses numpy's complex exponential, not the cached table, so the
+    tolerance covers the table's float32 rounding."""
+    g = torch.Generator().manual_seed(32)
+    N, H, d = 9, 3, 16
+    x = rnd((N, H, d), g)
+    pos = torch.randint(0, 60, (N,), generator=g).numpy().astype(np.int32)
+    out = orc.rope(x, pos, _cos_sin_table(d, 64))
+    xf = f64(x).numpy()
+    z = xf[..., : d // 2] + 1j * xf[..., d // 2:]
+    w = z * np.exp(1j * _angles(d, pos))[:, None, :]
+    ref = np.concatenate([w.real, w.imag], -1)
+    assert np.abs(out - ref).max() <= 1e-6 * (np.abs(xf).max() + 1.0), "not a rotation by +theta"
+
+
+def pin_rope_relative_position(orc):
+    """<R(p) q, R(p') k> depends on p - p' only (the property RoPE exists for)."""
+    g = torch.Generator().manual_seed(33)
+    d = 32
+    q = rnd((1, 1, d), g)
+    k = rnd((1, 1, d), g)
+    table = _cos_sin_table(d, 256)
+    one = lambda x, p: orc.rope(x, np.array([p], dtype=np.int32), table).reshape(d)
+    scale = float(torch.linalg.norm(f64(q)) * torch.linalg.norm(f64(k)))
+    for p, pp, delta in ((3, 10, 17), (40, 2, 100), (0, 0, 200), (7, 7, 1)):
+        a = float(np.dot(one(q, p), one(k, pp)))
+        b = float(np.dot(one(q, p + delta), one(k, pp + delta)))
+        assert abs(a - b) <= 1e-5 * scale, ("relative position", p, pp, delta)
+    # and it does depend on the offset
+    assert abs(float(np.dot(one(q, 0), one(k, 0))) - float(np.dot(one(q, 0), one(k, 5)))) > 1e-3 * scale
+
+
+def pin_rope_rejects_positions_outside_table(orc):
+    x = rnd((2, 1, 8), torch.Generator().manual_seed(34))
+    for bad in ([0, 4], [-1, 0]):
+        try:
+            orc.rope(x, np.array(bad, dtype=np.int32), _cos_sin_table(8, 4))
+        except ValueError:
+            continue
+        raise AssertionError("a position outside the table was accepted")
+
+
 ALL_PINS = [
     pin_store_kv_index_put,
     pin_single_token_returns_v,
@@ -422,4 +490,8 @@ ALL_PINS = [
     pin_extend_prefix_sharing,
     pin_dummy_requests,
     pin_golden_page_table_example,
+    pin_rope_position_zero_is_identity,
+    pin_rope_is_complex_rotation,
+    pin_rope_relative_position,
+    pin_rope_rejects_positions_outside_table,
 ]

@@ -41,6 +41,16 @@ MUTATIONS = [
      "memcpy(k_pool + row * pool_row_stride, v + i * tok_stride"),
     ("merge-unweighted", "o[c] += w * os[c];", "o[c] += os[c];"),
     ("merge-lse-no-max", "lse_out[i] = top + log(total);", "lse_out[i] = log(total);"),
+    ("rope-first-half-sign", "out[at + j] = x1 * c - x2 * s;", "out[at + j] = x1 * c + x2 * s;"),
+    ("rope-second-half-sign", "out[at + half + j] = x2 * c + x1 * s;",
+     "out[at + half + j] = x2 * c - x1 * s;"),
+    ("rope-adjacent-pairs", "x2 = widen(x[at + half + j]);", "x2 = widen(x[at + (j ^ 1)]);"),
+    ("rope-cos-sin-swapped", "const double c = (double)cs[j], s = (double)cs[half + j];",
+     "const double s = (double)cs[j], c = (double)cs[half + j];"),
+    ("rope-position-off-by-one", "cos_sin_cache + pos * head_dim;", "cos_sin_cache + (pos + 1) * head_dim;"),
+    ("rope-heads-transposed", "const int64_t at = (i * num_heads + h) * (int64_t)head_dim;",
+     "const int64_t at = (h * n_tokens + i) * (int64_t)head_dim;"),
+    ("rope-no-range-check", "if (pos < 0 || pos >= max_positions)", "if (pos < 0)"),
     ("weights-skip-first", "for (int64_t j = j0; j < j1; j++) {\n        double w",
      "for (int64_t j = j0 + 1; j < j1; j++) {\n        double w"),
 ]

@@ -357,3 +357,35 @@ def make_extend_values(case: ExtendCase, device: str = "cpu"):
                                  device=device), case.value_std, g)
         per_batch.append((k, v, q))
     return pool, per_batch
+
+
+# --------------------------------------------------------------------------- #
+# rotary position embedding inputs
+# --------------------------------------------------------------------------- #
+def rope_cos_sin_cache(head_dim: int, max_positions: int, base: float = 10000.0) -> torch.Tensor:
+    """The cos/sin table a serving engine builds once at start-up for RoPE
+    ("mini-sglang architecture deep dive", section 7.3): row p holds
+    [cos(p f_0) .. cos(p f_{d/2-1}), sin(p f_0) .. sin(p f_{d/2-1})] with
+    f_i = base^(-2i/d), in float32 (rotary_dim = head_dim).  It is an input to
+    the RoPE step, like the pool; the pages give no base, 10000 is used."""
+    freq = 1.0 / (base ** (torch.arange(0, head_dim, 2, dtype=torch.float32) / head_dim))
+    ang = torch.outer(torch.arange(max_positions, dtype=torch.float32), freq)
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).contiguous()
+
+
+def decode_positions(case: DecodeCase) -> torch.Tensor:
+    """Position of the token each request stores this step: its context
+    length minus one (the context includes that token).  Padding requests
+    all use position 0, so their rotated keys agree byte for byte."""
+    pos = (case.seq_lens - 1).clamp(min=0).to(torch.int32)
+    if case.num_real < case.batch:
+        pos[case.num_real:] = 0
+    return pos
+
+
+def extend_positions(batch: ExtendBatch) -> torch.Tensor:
+    """Positions of the packed new tokens of an extend batch: request r's new
+    token t sits at cached_len[r] + t."""
+    parts = [torch.arange(int(c), int(c) + int(e), dtype=torch.int32)
+             for c, e in zip(batch.cached_lens.tolist(), batch.extend_lens.tolist())]
+    return torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int32)
