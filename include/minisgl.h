@@ -7,6 +7,7 @@
  *   minisgl_store_kv     scatter this step's new K/V token rows into the pool
  *   minisgl_decode_attn  one query token per request, split-KV, then an LSE merge
  *   minisgl_extend_attn  causal attention for the new tokens of chunked prefill
+ *   minisgl_rope_store_kv  rotary position embedding of q and k fused with store_kv
  *
  * Sources of the definitions (page title, section):
  *   [deep-dive]  "mini-sglang 架构深度解读" (mini-sglang architecture deep dive,
@@ -181,6 +182,37 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
                         const int32_t *extend_lens, const int32_t *q_offsets,
                         int32_t total_q_tokens, float sm_scale, void *out, void *stream);
+
+/*
+ * Rotary position embedding fused with store_kv [deep-dive 7.3 RoPE: a
+ * float32 [cos | sin] table per position, rotary_dim = head_dim, q and k
+ * rotated in place by each token's position; learn, paged KV pool: store_kv
+ * then scatters the new K/V rows].  For token i < n_tokens at position
+ * p = positions[i], every head x of q and of k is rotated pairwise, element j
+ * with element j + d/2 (the half-split pairing; the pages name the library
+ * call but not the pairing):
+ *     y[j]       = x[j] * cos_j(p) - x[j + d/2] * sin_j(p)
+ *     y[j + d/2] = x[j + d/2] * cos_j(p) + x[j] * sin_j(p),     j < d/2,
+ * with cos_j(p) = cos_sin_cache[p*d + j], sin_j(p) = cos_sin_cache[p*d + d/2 + j].
+ * Arithmetic in fp32 from the bf16 inputs, results rounded to nearest bf16.
+ *   q: device bf16, token i's heads at q + i*q_tok_stride, [num_q_heads, d];
+ *      overwritten with the rotated q.
+ *   k, v: device bf16 [n_tokens, H_kv, d] rows (token strides in elements);
+ *      read only.  The rotated k is written to K[layer][out_loc[i]] and v to
+ *      V[layer][out_loc[i]] (v bit-exact); k itself is not rotated in place.
+ *   positions, out_loc: device int32 [n_tokens].
+ *   cos_sin_cache: device float32 [max_positions, d], 16-byte aligned.
+ * Positions outside [0, max_positions) and rows outside [0, num_rows) are a
+ * caller error: they are clamped into range (results unspecified), never
+ * trapped.  Tokens sharing a row (CUDA-Graph padding) race as in
+ * minisgl_store_kv; give them identical k, v and positions.
+ * head_dim 64 or 128.  n_tokens == 0 is a no-op.
+ */
+int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, int32_t num_q_heads,
+                          int64_t q_tok_stride, const void *k, const void *v, int64_t k_tok_stride,
+                          int64_t v_tok_stride, const int32_t *positions, const float *cos_sin_cache,
+                          int32_t max_positions, const int32_t *out_loc, int32_t n_tokens,
+                          void *stream);
 
 /*
  * Decode attention that allocates nothing (no counterpart in the pages; this

@@ -9,6 +9,7 @@ Entry points (same names as the C ABI):
     minisgl_store_kv(pool, layer, k, v, out_loc)
     minisgl_decode_attn(pool, layer, q, page_table, seq_lens, sm_scale, ...)
     minisgl_extend_attn(pool, layer, q, page_table, cached_lens, extend_lens, q_offsets, sm_scale, ...)
+    minisgl_rope_store_kv(pool, layer, q, k, v, positions, cos_sin_cache, out_loc)
 """
 from __future__ import annotations
 
@@ -24,13 +25,13 @@ __all__ = [
     "KVPool", "minisgl_store_kv", "minisgl_decode_attn", "minisgl_extend_attn",
     "minisgl_decode_workspace_bytes", "minisgl_device_sm_count", "minisgl_debug_timeout_count",
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
-    "minisgl_decode_attn_noalloc",
+    "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
 ]
 
 EXPORTED_SYMBOLS = [
     "minisgl_store_kv", "minisgl_decode_workspace_bytes", "minisgl_decode_attn",
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
-    "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc",
+    "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
 ]
 
 MINISGL_BF16 = 1
@@ -74,6 +75,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_decode_attn_noalloc.restype = ctypes.c_int
     lib.minisgl_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, f32, vp, vp]
     lib.minisgl_extend_attn.restype = ctypes.c_int
+    lib.minisgl_rope_store_kv.argtypes = [P, i32, vp, i32, i64, vp, vp, i64, i64, vp, vp, i32, vp,
+                                          i32, vp]
+    lib.minisgl_rope_store_kv.restype = ctypes.c_int
     lib.minisgl_last_error.argtypes = []
     lib.minisgl_last_error.restype = ctypes.c_char_p
     lib.minisgl_device_sm_count.argtypes = []
@@ -278,3 +282,34 @@ def minisgl_debug_timeout_count() -> int:
     c = ctypes.c_uint32(0)
     _check(load_library().minisgl_debug_timeout_count(ctypes.byref(c)), "debug_timeout_count")
     return int(c.value)
+
+
+def minisgl_rope_store_kv(pool: KVPool, layer: int, q: torch.Tensor, k: torch.Tensor,
+                          v: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                          out_loc: torch.Tensor, stream=None) -> torch.Tensor:
+    """Rotate q [N, H_q, d] in place and k [N, H_kv, d] into the pool by each
+    token's position, and store v; returns q.  k is left unrotated."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16)
+    _need(positions, "positions", torch.int32)
+    _need(out_loc, "out_loc", torch.int32)
+    _need(cos_sin_cache, "cos_sin_cache", torch.float32)
+    n = out_loc.numel()
+    d = pool.head_dim
+    if q.dim() != 3 or q.shape[0] != n or q.shape[2] != d or q.stride(2) != 1 or q.stride(1) != d:
+        raise MinisglError("q must be [n_tokens, H_q, head_dim] with contiguous rows")
+    for t, nm in ((k, "k"), (v, "v")):
+        if (t.dim() != 3 or t.shape[0] != n or t.shape[1] != pool.num_kv_heads or t.shape[2] != d
+                or t.stride(2) != 1 or t.stride(1) != d):
+            raise MinisglError(f"{nm} must be [n_tokens, H_kv, d] with contiguous rows")
+    if positions.numel() != n or not positions.is_contiguous() or not out_loc.is_contiguous():
+        raise MinisglError("positions and out_loc must be contiguous [n_tokens]")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != d or not cos_sin_cache.is_contiguous():
+        raise MinisglError("cos_sin_cache must be contiguous [max_positions, head_dim] float32")
+    _check(lib.minisgl_rope_store_kv(ctypes.byref(pool.desc), layer, _ptr(q), q.shape[1], q.stride(0),
+                                     _ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(positions),
+                                     _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(out_loc), n,
+                                     _stream(stream)), "rope_store_kv")
+    return q

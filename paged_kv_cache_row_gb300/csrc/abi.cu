@@ -248,4 +248,48 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
     return cuda_status(minisgl::launch_extend(a, static_cast<cudaStream_t>(stream)), "extend_attn");
 }
 
+int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, int32_t num_q_heads,
+                          int64_t q_tok_stride, const void *k, const void *v, int64_t k_tok_stride,
+                          int64_t v_tok_stride, const int32_t *positions, const float *cos_sin_cache,
+                          int32_t max_positions, const int32_t *out_loc, int32_t n_tokens,
+                          void *stream) {
+    g_err.clear();
+    if (int rc = check_pool(pool, layer, "rope_store_kv")) return rc;
+    if (num_q_heads < 1) return fail(MINISGL_ERR_ARG, "rope_store_kv: num_q_heads < 1");
+    if (n_tokens < 0) return fail(MINISGL_ERR_ARG, "rope_store_kv: n_tokens < 0");
+    if (max_positions < 1) return fail(MINISGL_ERR_ARG, "rope_store_kv: max_positions < 1");
+    if (n_tokens == 0) return MINISGL_OK;
+    if (!q || !k || !v || !positions || !cos_sin_cache || !out_loc)
+        return fail(MINISGL_ERR_ARG, "rope_store_kv: NULL pointer argument");
+    const int64_t d = pool->head_dim;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cos_sin_cache))
+        return fail(MINISGL_ERR_SHAPE, "rope_store_kv: q, k, v and the cos/sin table must be 16-byte aligned");
+    if (q_tok_stride < (int64_t)num_q_heads * d || q_tok_stride % 8)
+        return fail(MINISGL_ERR_SHAPE, "rope_store_kv: q token stride must be >= H_q*d and a multiple of 8");
+    const int64_t row = (int64_t)pool->num_kv_heads * d;
+    if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+        return fail(MINISGL_ERR_SHAPE, "rope_store_kv: k/v token strides must be >= H_kv*d and multiples of 8");
+    minisgl::RopeStoreArgs a;
+    a.k_layer = const_cast<void *>(layer_ptr(pool->k_base, pool, layer));
+    a.v_layer = const_cast<void *>(layer_ptr(pool->v_base, pool, layer));
+    a.row_stride = pool->row_stride;
+    a.num_rows = pool->num_rows;
+    a.q = q;
+    a.q_tok_stride = q_tok_stride;
+    a.k = k;
+    a.v = v;
+    a.k_tok_stride = k_tok_stride;
+    a.v_tok_stride = v_tok_stride;
+    a.positions = positions;
+    a.cos_sin = cos_sin_cache;
+    a.max_positions = max_positions;
+    a.out_loc = out_loc;
+    a.n_tokens = n_tokens;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = pool->num_kv_heads;
+    a.head_dim = (int32_t)d;
+    return cuda_status(minisgl::launch_rope_store_kv(a, static_cast<cudaStream_t>(stream)),
+                       "rope_store_kv");
+}
+
 }  // extern "C"

@@ -72,6 +72,22 @@ struct ExtendArgs {
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s);
 
+struct RopeStoreArgs {
+    void *k_layer, *v_layer;      // layer base of K / V in the pool
+    int64_t row_stride;           // elements between pool rows
+    int32_t num_rows;
+    void *q;                      // [N, H_q, D], rotated in place
+    int64_t q_tok_stride;
+    const void *k, *v;            // new rows [N, H_kv, D]
+    int64_t k_tok_stride, v_tok_stride;
+    const int32_t *positions;     // [N]
+    const float *cos_sin;         // [max_positions, D]: cos | sin
+    int32_t max_positions;
+    const int32_t *out_loc;       // [N]
+    int32_t n_tokens, num_q_heads, num_kv_heads, head_dim;
+};
+cudaError_t launch_rope_store_kv(const RopeStoreArgs &a, cudaStream_t s);
+
 int device_sm_count();
 
 // Sets the calling thread's minisgl_last_error() message and returns `code`.

@@ -91,6 +91,14 @@ def test_error_codes_on_host(lib):
                                    -0.1, fake, None) == -1
     assert lib.minisgl_extend_attn(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
                                    float("nan"), fake, None) == -1
+    # rope_store_kv: q stride below H_q*d, unaligned table, no table rows, NULL positions
+    rs = lib.minisgl_rope_store_kv
+    assert rs(ref(d), 0, fake, 16, 1024, fake, fake, 1024, 1024, fake, fake, 64, fake, 4, None) == -3
+    assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, fake, fake + 4, 64, fake, 4, None) == -3
+    assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, fake, fake, 0, fake, 4, None) == -1
+    assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, None, fake, 64, fake, 4, None) == -1
+    assert rs(ref(d), 0, fake, 0, 2048, fake, fake, 1024, 1024, fake, fake, 64, fake, 4, None) == -1
+    assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, fake, fake, 64, fake, 0, None) == 0
     # empty work is a no-op that touches nothing
     assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 1024, 1024, fake, 0, None) == 0
     assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 0, 32, 32, fake, 0.1, fake, fake,
