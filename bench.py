@@ -57,6 +57,16 @@ def store_layer_bytes(case) -> int:
     return case.batch * (2 * 2 * case.num_kv_heads * case.head_dim * 2 + 4)
 
 
+def cascade_layer_bytes(case) -> int:
+    """Shared-prefix decode reading the shared rows once: the prefix K/V and
+    its page-table entries once, each request's private rows and entries,
+    the queries, outputs and seq_lens."""
+    Hkv, d, Hq = case.num_kv_heads, case.head_dim, case.num_q_heads
+    P = case.shared_len
+    own = int((case.seq_lens - P).clamp(min=0).sum())
+    return ((P + own) * (2 * Hkv * d * 2 + 4) + case.batch * Hq * d * 2 * 2 + case.batch * 4)
+
+
 def rope_store_bytes(case) -> int:
     """Fused RoPE + store_kv over all extend batches: per token, q read and
     written, k and v read and written to the pool, one cos/sin row, the
@@ -322,6 +332,46 @@ def run_gpu(args, world, rank, local):
     peak = peaks["hbm_gbs"]
     traffic = profile_traffic("decode.cu", "decode_qwen3_0p6b.md")
 
+    # ---- shared-prefix (cascade) decode vs plain decode on one radix-shared batch ----
+    casc = None
+    if not args.no_extend:
+        sc = workloads.decode_shared_prefix_qwen3()
+        spool_t, sk, sv, sq = workloads.make_decode_values(sc, dev)
+        spool = mk.KVPool(spool_t)
+        spt, ssl, sloc = sc.page_table.to(dev), sc.seq_lens.to(dev), sc.out_loc.to(dev)
+        mk.minisgl_store_kv(spool, 0, sk[0], sv[0], sloc)
+        sout = torch.empty_like(sq[0])
+        flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+        runs = {
+            "cascade": lambda: mk.minisgl_cascade_decode_attn(spool, 0, sq[0], spt, ssl, sc.shared_len,
+                                                              sc.sm_scale, out=sout),
+            "plain": lambda: mk.minisgl_decode_attn(spool, 0, sq[0], spt, ssl, sc.sm_scale, out=sout),
+        }
+        t_ms = {}
+        for nm, fn in runs.items():
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            evs = []
+            for _ in range(max(10, args.steps // 10)):
+                flush.zero_()  # the 4096-row prefix (33 MB) would otherwise stay in L2
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b_.record(stream)
+                evs.append((a, b_))
+            torch.cuda.synchronize()
+            t_ms[nm] = statistics.mean(a.elapsed_time(b_) for a, b_ in evs)
+        plain_b = decode_layer_bytes(sc)
+        casc_b = cascade_layer_bytes(sc)
+        casc = {"workload": sc.name, "ms_cascade": round(t_ms["cascade"], 5),
+                "ms_plain_decode": round(t_ms["plain"], 5),
+                "speedup": round(t_ms["plain"] / t_ms["cascade"], 3),
+                "algorithmic_bytes_cascade": casc_b, "algorithmic_bytes_plain": plain_b,
+                "achieved_gbs_cascade": round(casc_b / (t_ms["cascade"] * 1e-3) / 1e9, 1),
+                "l2": "flushed (256 MB write) before every timed call"}
+        del spool_t, sk, sv, sq, flush
+
     # ---- e2e: the same step through the C ABI with host buffers ----
     pin = lambda t: t.cpu().pin_memory()
     h_in = [pin(k_new), pin(v_new), pin(q), pin(case.page_table), pin(case.seq_lens), pin(case.out_loc)]
@@ -469,6 +519,7 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": gpu_launches,
         "extend": ext,
         "rope_store_kv": rope,
+        "cascade_decode": casc,
         "cpu_baseline": cpu,
     }
     if rank == 0:

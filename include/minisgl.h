@@ -8,6 +8,7 @@
  *   minisgl_decode_attn  one query token per request, split-KV, then an LSE merge
  *   minisgl_extend_attn  causal attention for the new tokens of chunked prefill
  *   minisgl_rope_store_kv  rotary position embedding of q and k fused with store_kv
+ *   minisgl_cascade_decode_attn  decode for requests sharing a prefix, prefix read once
  *
  * Sources of the definitions (page title, section):
  *   [deep-dive]  "mini-sglang 架构深度解读" (mini-sglang architecture deep dive,
@@ -182,6 +183,38 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
                         const int32_t *extend_lens, const int32_t *q_offsets,
                         int32_t total_q_tokens, float sm_scale, void *out, void *stream);
+
+/*
+ * Workspace size, in bytes, for minisgl_cascade_decode_attn with this batch
+ * and head shape (room for up to 32 prefix chunks and 16 suffix splits); 0
+ * for invalid sizes.
+ */
+size_t minisgl_cascade_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim);
+
+/*
+ * Decode attention for a batch whose requests share a cached prefix
+ * [learn, radix-cache chapter: requests matching a cached prefix point at its
+ * rows; deep-dive 5.3 PagedAttention].  Same definition and arguments as
+ * minisgl_decode_attn, plus shared_len = P: the caller guarantees that the
+ * first P page-table entries are the same physical rows in every row of the
+ * batch and that every seq_lens[r] >= P (results are unspecified otherwise;
+ * nothing is checked on the device).  The shared rows are read once per KV
+ * head for the whole batch instead of once per request: the P prefix
+ * positions are attended by all B*G query rows of a KV head at once on the
+ * tensor cores (in chunks spread over the SMs), each request's own positions
+ * [P, seq_len) by the split-KV decode kernels, and the parts are merged by
+ * their log-sum-exp.
+ * workspace: device, 256-byte aligned, at least
+ *   minisgl_cascade_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim) bytes.
+ * Supported: head_dim 128; num_q_heads/num_kv_heads in {1, 2, 4, 8, 16};
+ * 1 <= shared_len <= pt_width; batch <= 4096.
+ */
+int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                                int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                                int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
+                                int32_t shared_len, float sm_scale, void *out, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * Rotary position embedding fused with store_kv [deep-dive 7.3 RoPE: a

@@ -25,13 +25,15 @@ __all__ = [
     "KVPool", "minisgl_store_kv", "minisgl_decode_attn", "minisgl_extend_attn",
     "minisgl_decode_workspace_bytes", "minisgl_device_sm_count", "minisgl_debug_timeout_count",
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
-    "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
+    "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv", "minisgl_cascade_decode_attn",
+    "minisgl_cascade_workspace_bytes",
 ]
 
 EXPORTED_SYMBOLS = [
     "minisgl_store_kv", "minisgl_decode_workspace_bytes", "minisgl_decode_attn",
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
     "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
+    "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes",
 ]
 
 MINISGL_BF16 = 1
@@ -78,6 +80,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_rope_store_kv.argtypes = [P, i32, vp, i32, i64, vp, vp, i64, i64, vp, vp, i32, vp,
                                           i32, vp]
     lib.minisgl_rope_store_kv.restype = ctypes.c_int
+    lib.minisgl_cascade_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.minisgl_cascade_workspace_bytes.restype = sz
+    lib.minisgl_cascade_decode_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, i32, f32, vp,
+                                                vp, sz, vp]
+    lib.minisgl_cascade_decode_attn.restype = ctypes.c_int
     lib.minisgl_last_error.argtypes = []
     lib.minisgl_last_error.restype = ctypes.c_char_p
     lib.minisgl_device_sm_count.argtypes = []
@@ -313,3 +320,43 @@ def minisgl_rope_store_kv(pool: KVPool, layer: int, q: torch.Tensor, k: torch.Te
                                      _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(out_loc), n,
                                      _stream(stream)), "rope_store_kv")
     return q
+
+
+def minisgl_cascade_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int,
+                                    head_dim: int) -> int:
+    return int(load_library().minisgl_cascade_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                              head_dim))
+
+
+def minisgl_cascade_decode_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: torch.Tensor,
+                                seq_lens: torch.Tensor, shared_len: int, sm_scale: float,
+                                out: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention of q [B, H_q, d] for requests whose first shared_len
+    page-table entries are the same rows; the shared rows are read once."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16)
+    _need(page_table, "page_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, Hq, d = q.shape
+    if not q.is_contiguous() or d != pool.head_dim:
+        raise MinisglError("q must be contiguous [B, H_q, head_dim]")
+    if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if seq_lens.numel() != B or not seq_lens.is_contiguous():
+        raise MinisglError("seq_lens must be contiguous [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16)
+    if workspace is None:
+        nbytes = minisgl_cascade_workspace_bytes(B, Hq, pool.num_kv_heads, d)
+        key = ("cascade", q.device, nbytes)
+        workspace = _ws_cache.get(key)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+            _ws_cache[key] = workspace
+    _check(lib.minisgl_cascade_decode_attn(ctypes.byref(pool.desc), layer, _ptr(q), Hq, _ptr(page_table),
+                                           B, page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
+                                           int(shared_len), float(sm_scale), _ptr(out), _ptr(workspace),
+                                           workspace.numel(), _stream(stream)), "cascade_decode_attn")
+    return out

@@ -3,6 +3,7 @@
 // Host-side argument checks, the thread-local error string, workspace
 // carving, and the launches.  No entry point allocates device memory or
 // synchronises with the device.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -200,6 +201,7 @@ int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
     a.ws_o = reinterpret_cast<float *>(ws);
     a.max_splits = splits;
     a.split_tokens = split_tokens;
+    a.lse_out = nullptr;
     return cuda_status(minisgl::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode_attn");
 }
 
@@ -245,7 +247,148 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
     a.head_dim = pool->head_dim;
     a.sm_scale = sm_scale;
     a.out = out;
+    a.prefix_only = 0;
+    a.out_f32 = nullptr;
+    a.lse_out = nullptr;
+    a.out_offsets = nullptr;
     return cuda_status(minisgl::launch_extend(a, static_cast<cudaStream_t>(stream)), "extend_attn");
+}
+
+}  // extern "C"
+
+namespace {
+
+constexpr int CASCADE_MAX_CHUNKS = 32;
+
+constexpr int CASCADE_SUFFIX_SPLITS = 16;
+
+// Workspace layout of minisgl_cascade_decode_attn (each part 256-byte aligned):
+// int32 metadata (4 arrays of chunks+1, one of batch), fp32 prefix partials
+// [chunks, B, Hq, D] and their LSEs [chunks, B, Hq], the bf16 suffix result
+// [B, Hq, D] and its LSEs [B, Hq], then a decode workspace for the suffix.
+size_t cascade_bytes(int64_t batch, int64_t hq, int64_t hkv, int64_t d, int64_t chunks) {
+    return align256((size_t)(4 * (chunks + 1) + batch) * 4) +
+           align256((size_t)chunks * batch * hq * d * 4) + align256((size_t)chunks * batch * hq * 4) +
+           align256((size_t)batch * hq * d * 2) + align256((size_t)batch * hq * 4) +
+           ws_bytes(batch, hq, hkv, d, CASCADE_SUFFIX_SPLITS);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t minisgl_cascade_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim) {
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1) return 0;
+    return cascade_bytes(batch, num_q_heads, num_kv_heads, head_dim, CASCADE_MAX_CHUNKS);
+}
+
+int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                                int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                                int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
+                                int32_t shared_len, float sm_scale, void *out, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    g_err.clear();
+    if (int rc = check_pool(pool, layer, "cascade_decode_attn")) return rc;
+    if (pool->head_dim != 128)
+        return fail(MINISGL_ERR_UNSUPPORTED, "cascade_decode_attn: head_dim %d (only 128)", pool->head_dim);
+    if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "cascade_decode_attn")) return rc;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if (G & (G - 1))
+        return fail(MINISGL_ERR_UNSUPPORTED, "cascade_decode_attn: group size %d not a power of 2", G);
+    if (batch < 0 || batch > 4096)
+        return fail(MINISGL_ERR_ARG, "cascade_decode_attn: batch %d outside [0, 4096]", batch);
+    if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f))
+        return fail(MINISGL_ERR_ARG, "cascade_decode_attn: sm_scale must be positive and finite");
+    if (pt_width < 1 || pt_row_stride < pt_width)
+        return fail(MINISGL_ERR_SHAPE, "cascade_decode_attn: need 1 <= pt_width <= pt_row_stride");
+    if (shared_len < 1 || shared_len > pt_width)
+        return fail(MINISGL_ERR_ARG, "cascade_decode_attn: shared_len %d outside [1, pt_width]", shared_len);
+    if (batch == 0) return MINISGL_OK;
+    if (!q || !page_table || !seq_lens || !out || !workspace)
+        return fail(MINISGL_ERR_ARG, "cascade_decode_attn: NULL pointer argument");
+    if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MINISGL_ERR_SHAPE, "cascade_decode_attn: q, out 16-byte and workspace 256-byte aligned");
+    // prefix chunks: about two work items per SM, at least four 128-token tiles each
+    const int64_t tiles = (shared_len + 127) / 128;
+    const int64_t tq2 = 2 * (128 / G);
+    const int64_t items_per_chunk = ((batch + tq2 - 1) / tq2) * pool->num_kv_heads;
+    int64_t chunks = (2 * (int64_t)minisgl::device_sm_count() + items_per_chunk - 1) / items_per_chunk;
+    chunks = std::max<int64_t>(1, std::min<int64_t>({chunks, (tiles + 3) / 4, (int64_t)CASCADE_MAX_CHUNKS}));
+    const int64_t chunk_len = ((tiles + chunks - 1) / chunks) * 128;
+    chunks = (shared_len + chunk_len - 1) / chunk_len;
+    const int64_t Hkv = pool->num_kv_heads, d = pool->head_dim;
+    const size_t need = cascade_bytes(batch, num_q_heads, Hkv, d, chunks);
+    if (workspace_bytes < need)
+        return fail(MINISGL_ERR_WORKSPACE, "cascade_decode_attn: workspace %zu bytes < %zu", workspace_bytes,
+                    need);
+    minisgl::ExtendArgs base;
+    base.q = q;
+    base.k_layer = layer_ptr(pool->k_base, pool, layer);
+    base.v_layer = layer_ptr(pool->v_base, pool, layer);
+    base.row_stride = pool->row_stride;
+    base.num_rows = pool->num_rows;
+    base.num_q_heads = num_q_heads;
+    base.num_kv_heads = pool->num_kv_heads;
+    base.head_dim = pool->head_dim;
+    base.sm_scale = sm_scale;
+    base.out = nullptr;
+    minisgl::CascadeArgs c;
+    char *ws = static_cast<char *>(workspace);
+    int32_t *meta = reinterpret_cast<int32_t *>(ws);
+    const int64_t S1 = chunks + 1;
+    c.meta.pre_cached = meta;
+    c.meta.pre_extend = meta + S1;
+    c.meta.pre_qoff = meta + 2 * S1;
+    c.meta.pre_ooff = meta + 3 * S1;
+    c.meta.suf_seq = meta + 4 * S1;
+    ws += align256((size_t)(4 * S1 + batch) * 4);
+    const size_t vec = (size_t)batch * num_q_heads;
+    c.pre_o = reinterpret_cast<float *>(ws);
+    ws += align256((size_t)chunks * vec * d * 4);
+    c.pre_lse = reinterpret_cast<float *>(ws);
+    ws += align256((size_t)chunks * vec * 4);
+    c.suf_out = ws;
+    ws += align256(vec * d * 2);
+    c.suf_lse = reinterpret_cast<float *>(ws);
+    ws += align256(vec * 4);
+    c.page_table = page_table;
+    c.pt_row_stride = pt_row_stride;
+    c.pt_width = pt_width;
+    c.seq_lens = seq_lens;
+    c.batch = batch;
+    c.num_q_heads = num_q_heads;
+    c.head_dim = pool->head_dim;
+    c.shared_len = shared_len;
+    c.chunks = (int32_t)chunks;
+    c.chunk_len = (int32_t)chunk_len;
+    c.out = out;
+    minisgl::DecodeArgs &sd = c.suffix;  // the suffix: page table shifted by P columns
+    sd.q = q;
+    sd.k_layer = base.k_layer;
+    sd.v_layer = base.v_layer;
+    sd.row_stride = pool->row_stride;
+    sd.num_rows = pool->num_rows;
+    sd.page_table = page_table + shared_len;
+    sd.pt_stride = pt_row_stride;
+    sd.pt_width = pt_width - shared_len;
+    sd.seq_lens = c.meta.suf_seq;
+    sd.batch = batch;
+    sd.num_q_heads = num_q_heads;
+    sd.num_kv_heads = pool->num_kv_heads;
+    sd.head_dim = pool->head_dim;
+    sd.sm_scale = sm_scale;
+    sd.out = c.suf_out;
+    sd.split_count = reinterpret_cast<int32_t *>(ws);
+    ws += align256((size_t)batch * Hkv * 4);
+    sd.ws_lse = reinterpret_cast<float *>(ws);
+    ws += align256(vec * CASCADE_SUFFIX_SPLITS * 4);
+    sd.ws_o = reinterpret_cast<float *>(ws);
+    sd.max_splits = CASCADE_SUFFIX_SPLITS;
+    sd.split_tokens = 0;
+    sd.lse_out = c.suf_lse;
+    return cuda_status(minisgl::launch_cascade(c, base, static_cast<cudaStream_t>(stream)),
+                       "cascade_decode_attn");
 }
 
 int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, int32_t num_q_heads,

@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
                     const float inv = 1.f / lt;
                     const int64_t hh = (int64_t)cur_r * Hq + cur_g * G + h;
                     if (whole) {
+                        if (a.lse_out && dr == 0) a.lse_out[hh] = (m[n][e] + __log2f(lt)) * LN2;
                         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + hh * D + dr;
 #pragma unroll
                         for (int mt = 0; mt < C::MT; ++mt) {
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     if (n == 0) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) out[c] = __float2bfloat16_rn(0.f);
+        if (a.lse_out && lane == 0) a.lse_out[wid] = -INFINITY;
         return;
     }
     const int S = min(a.split_count[(int64_t)r * Hkv + g], a.max_splits);
@@ -423,6 +425,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (a.lse_out && lane == 0) a.lse_out[wid] = M + __logf(tot);
     const float inv = 1.f / tot;
 #pragma unroll
     for (int c = 0; c < CPL; c += 2)

@@ -176,12 +176,12 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
 
 // One work item: request r, KV head g, query tiles A (new tokens t0 ..
 // ta_last) and B (t0 + TQ .. tb_last, when live_b), C cached tokens before
-// them; nkv_a / nkv_b KV tiles seen by each tile.
+// them; nkv_a / nkv_b KV tiles seen by each tile; vis KV positions read.
 struct Item {
-    int r, g, t0, ta_last, tb_last, C, qoff, nkv_a, nkv_b;
+    int r, g, t0, ta_last, tb_last, C, qoff, ooff, nkv_a, nkv_b, vis;
     bool live_b;
     __device__ __forceinline__ int nkv() const { return max(nkv_a, nkv_b); }
-    __device__ __forceinline__ int n_vis() const { return C + tb_last + 1; }  // KV positions seen
+    __device__ __forceinline__ int n_vis() const { return vis; }
 };
 
 // Work item `item` from the per-request prefix of item counts in shared
@@ -201,14 +201,24 @@ __device__ __forceinline__ Item load_item(const ExtendArgs &a, const int32_t *s_
     const int qb = off - it.g * nqb;
     const int W = a.pt_width;
     it.C = min(max(__ldg(a.cached_lens + lo), 0), W);
-    const int E = min(max(__ldg(a.extend_lens + lo), 0), W - it.C);
+    // (in prefix-only mode a new token is not a page-table position)
+    const int E = a.prefix_only ? max(__ldg(a.extend_lens + lo), 0)
+                                : min(max(__ldg(a.extend_lens + lo), 0), W - it.C);
     it.qoff = __ldg(a.q_offsets + lo);
+    it.ooff = a.out_offsets ? __ldg(a.out_offsets + lo) : it.qoff;
     it.t0 = qb * 2 * TQ;
     it.ta_last = min(it.t0 + TQ, E) - 1;
     it.live_b = it.t0 + TQ < E;
     it.tb_last = it.live_b ? min(it.t0 + 2 * TQ, E) - 1 : it.ta_last;
-    it.nkv_a = (it.C + it.ta_last + 1 + ROWS - 1) / ROWS;
-    it.nkv_b = it.live_b ? (it.C + it.tb_last + 1 + ROWS - 1) / ROWS : 0;
+    if (a.prefix_only) {  // every new token sees exactly the C cached positions
+        it.vis = it.C;
+        it.nkv_a = (it.C + ROWS - 1) / ROWS;
+        it.nkv_b = it.live_b ? it.nkv_a : 0;
+    } else {              // causal: token t sees C + t + 1 positions
+        it.vis = it.C + it.tb_last + 1;
+        it.nkv_a = (it.C + it.ta_last + 1 + ROWS - 1) / ROWS;
+        it.nkv_b = it.live_b ? (it.C + it.tb_last + 1 + ROWS - 1) / ROWS : 0;
+    }
     return it;
 }
 
@@ -271,8 +281,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             int v = 0;
             if (r < B) {
                 const int c = min(max(__ldg(a.cached_lens + r), 0), W);
-                const int e = min(max(__ldg(a.extend_lens + r), 0), W - c);
+                const int e = a.prefix_only ? max(__ldg(a.extend_lens + r), 0)
+                                            : min(max(__ldg(a.extend_lens + r), 0), W - c);
                 v = ((e + TQ2 - 1) / TQ2) * Hkv;
+                if (a.prefix_only && c == 0) v = 0;  // nothing to attend to: no items
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -493,7 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int tt = cur.t0 + x * TQ + (i >> log2g);
                 const bool live = tt <= t_last;
                 const int t = min(tt, t_last);
-                const int lim = cur.C + t;  // last visible position
+                const int lim = a.prefix_only ? cur.C - 1 : cur.C + t;  // last visible position
                 float m = -INFINITY;            // running max of scaled scores (base 2)
                 uint64_t l2 = f2(0.f, 0.f);     // running row sum, two partial lanes
                 for (int j = 0; j < nkv_x; ++j) {
@@ -564,14 +576,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 wait(pv_done(x), (cnt + nkv_x - 1) & 1);
                 tc_fence_after();
                 const float inv = 1.f / l;
-                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                     ((int64_t)(cur.qoff + t) * Hq + cur.g * G + (i & (G - 1))) * D;
+                const int64_t orow = (int64_t)(cur.ooff + t) * Hq + cur.g * G + (i & (G - 1));
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + orow * D;
+                if (a.out_f32 && live)  // natural-log LSE of the scaled scores
+                    a.lse_out[orow] = (m + log2f(l)) * 0.6931471805599453f;
 #pragma unroll 1
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t o[32];
                     tmem_ld32(ocol + 32 * q4, o);
                     tmem_wait_ld();
-                    if (live) {
+                    if (a.out_f32) {  // normalised fp32 rows for a later merge
+                        if (live) {
+                            float *fd = a.out_f32 + orow * D + 32 * q4;
+#pragma unroll
+                            for (int c = 0; c < 32; c += 4)
+                                *reinterpret_cast<float4 *>(fd + c) =
+                                    make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                                                __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                        }
+                    } else if (live) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             uint4 v;

@@ -54,6 +54,7 @@ struct DecodeArgs {
     float *ws_lse, *ws_o;
     int32_t max_splits;
     int32_t split_tokens;         // 0 = automatic
+    float *lse_out;               // optional [B, Hq] natural-log LSE of each output row
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 
@@ -68,9 +69,36 @@ struct ExtendArgs {
     const int32_t *cached_lens, *extend_lens, *q_offsets;
     int32_t batch, total_q_tokens, num_q_heads, num_kv_heads, head_dim;
     float sm_scale;
-    void *out;                    // [T, Hq, D] bf16
+    void *out;                    // [T, Hq, D] bf16 (unused when out_f32 is set)
+    int32_t prefix_only;          // 1: every new token sees exactly its C cached positions
+    float *out_f32;               // optional [T, Hq, D] fp32 normalised output
+    float *lse_out;               // [T, Hq] natural-log LSE, with out_f32
+    const int32_t *out_offsets;   // optional [B]: first output row of each request (else q_offsets)
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s);
+
+// Shared-prefix (cascade) decode: workspace-resident pseudo-request metadata
+// for the prefix-chunk extend launch, and the suffix decode's inputs/outputs.
+struct CascadeMeta {
+    int32_t *pre_cached, *pre_extend, *pre_qoff, *pre_ooff;  // [chunks] (+1 for qoff)
+    int32_t *suf_seq;                                         // [batch]: seq_len - P
+};
+struct CascadeArgs {
+    CascadeMeta meta;
+    const int32_t *page_table;    // [B, W]; the first shared_len columns equal in every row
+    int64_t pt_row_stride;
+    int32_t pt_width;
+    const int32_t *seq_lens;      // [B]
+    int32_t batch, num_q_heads, head_dim;
+    int32_t shared_len, chunks, chunk_len;
+    float *pre_o, *pre_lse;       // [chunks, B, Hq, D], [chunks, B, Hq]
+    void *suf_out;                // [B, Hq, D] bf16 suffix attention
+    float *suf_lse;               // [B, Hq]
+    DecodeArgs suffix;            // the suffix decode (workspace parts filled in by the caller)
+    void *out;                    // [B, Hq, D] bf16
+};
+// base: the extend arguments shared with the prefix launch (q, pool layer, heads, scale)
+cudaError_t launch_cascade(const CascadeArgs &c, const ExtendArgs &base, cudaStream_t s);
 
 struct RopeStoreArgs {
     void *k_layer, *v_layer;      // layer base of K / V in the pool

@@ -99,6 +99,15 @@ def test_error_codes_on_host(lib):
     assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, None, fake, 64, fake, 4, None) == -1
     assert rs(ref(d), 0, fake, 0, 2048, fake, fake, 1024, 1024, fake, fake, 64, fake, 4, None) == -1
     assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, fake, fake, 64, fake, 0, None) == 0
+    # cascade decode: shared_len outside [1, width], workspace too small, head_dim 64
+    cd = lib.minisgl_cascade_decode_attn
+    big = lib.minisgl_cascade_workspace_bytes(4, 16, 8, 128)
+    assert big > 0 and lib.minisgl_cascade_workspace_bytes(-1, 16, 8, 128) == 0
+    assert cd(ref(d), 0, fake, 16, fake, 4, 32, 32, fake, 0, 0.1, fake, fake, big, None) == -1
+    assert cd(ref(d), 0, fake, 16, fake, 4, 32, 32, fake, 33, 0.1, fake, fake, big, None) == -1
+    assert cd(ref(d), 0, fake, 16, fake, 4, 32, 32, fake, 16, 0.1, fake, fake, 1024, None) == -6
+    assert b"workspace" in lib.minisgl_last_error()
+    assert cd(ref(bad), 0, fake, 16, fake, 4, 32, 32, fake, 16, 0.1, fake, fake, big, None) == -4
     # empty work is a no-op that touches nothing
     assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 1024, 1024, fake, 0, None) == 0
     assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 0, 32, 32, fake, 0.1, fake, fake,

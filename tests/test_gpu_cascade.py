@@ -1,0 +1,91 @@
+"""GPU parity of the shared-prefix (cascade) decode call against the fp64 oracle.
+
+The oracle is plain decode over each request's full page-table row: cascade
+decode must compute exactly that, only reading the shared rows once.  Cases
+span group sizes 1-16, prefixes shorter than one tile, ending on and off tile
+edges, batches wider than one query block, empty private suffixes and the
+full 64-request, 4096-token-prefix workload of the benchmark.  All calls go
+through the C ABI (the ctypes binding).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_row_gb300 as mk
+import workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_row_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def run_cascade(case, shared_len, seq_override=None):
+    pool_t, k_new, v_new, q = workloads.make_decode_values(case, DEV)
+    hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+    pool = mk.KVPool(pool_t)
+    seq = case.seq_lens.clone() if seq_override is None else seq_override
+    pt, sl, loc = case.page_table.to(DEV), seq.to(DEV), case.out_loc.to(DEV)
+    mk.minisgl_store_kv(pool, 0, k_new[0], v_new[0], loc)
+    out = mk.minisgl_cascade_decode_attn(pool, 0, q[0], pt, sl, shared_len, case.sm_scale)
+    plain = mk.minisgl_decode_attn(pool, 0, q[0], pt, sl, case.sm_scale)
+    torch.cuda.synchronize()
+    orc = oracle.get()
+    orc.store_kv(hk, hv, k_new[0].cpu(), v_new[0].cpu(), case.out_loc)
+    ref, _ = orc.decode(q[0].cpu(), hk, hv, case.page_table, seq, case.sm_scale)
+    gu.check_attn(out, ref, f"{case.name} cascade")
+    gu.check_attn(plain, ref, f"{case.name} plain decode")
+    assert mk.minisgl_debug_timeout_count() == 0, "a tensor-core kernel wait ran out"
+    return out
+
+
+CASES = [
+    # Hq, Hkv, B, prefix, suffix_lo, suffix_hi
+    (8, 2, 5, 70, 0, 40),
+    (32, 8, 200, 300, 1, 700),
+    (64, 8, 9, 129, 0, 3),
+    (4, 4, 3, 128, 5, 5),
+    (32, 2, 7, 1, 1, 300),
+    (16, 8, 33, 1000, 0, 200),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,B,P,lo,hi", CASES)
+def test_cascade_decode_small(Hq, Hkv, B, P, lo, hi):
+    case = workloads.make_shared_prefix_decode_case(f"cascade-g{Hq // Hkv}-p{P}", num_q_heads=Hq,
+                                                    num_kv_heads=Hkv, head_dim=128, batch=B,
+                                                    prefix_len=P, suffix_lo=lo, suffix_hi=hi,
+                                                    seed=B * 31 + P)
+    run_cascade(case, P)
+
+
+def test_cascade_decode_empty_suffixes():
+    """Requests whose whole context is the shared prefix (no private rows):
+    only the prefix contributes."""
+    case = workloads.make_shared_prefix_decode_case("cascade-empty", num_q_heads=16, num_kv_heads=4,
+                                                    head_dim=128, batch=6, prefix_len=200,
+                                                    suffix_lo=0, suffix_hi=30, seed=3)
+    seq = case.seq_lens.clone()
+    seq[0] = 200
+    seq[3] = 200
+    run_cascade(case, 200, seq_override=seq)
+
+
+def test_cascade_decode_shared_len_shorter_than_sharing():
+    """Declaring fewer shared positions than the rows actually shared is
+    still exact (the rest is treated as private)."""
+    case = workloads.make_shared_prefix_decode_case("cascade-short", num_q_heads=8, num_kv_heads=8,
+                                                    head_dim=128, batch=4, prefix_len=400,
+                                                    suffix_lo=3, suffix_hi=90, seed=4)
+    run_cascade(case, 137)
+
+
+def test_cascade_decode_full_workload():
+    run_cascade(workloads.decode_shared_prefix_qwen3(), 4096)

@@ -91,6 +91,16 @@ def test_extend_edge_lengths():
     run_extend_case(_manual_case(cached, ext, seed=41))
 
 
+def test_extend_mixed_chunk_and_decode_batch():
+    """One extend launch carrying chunked-prefill requests and decode requests
+    (one new token over a long context) side by side, as a mixed batch does."""
+    g = torch.Generator().manual_seed(77)
+    n_dec = 24
+    cached = [0, 300, 1100] + torch.randint(100, 3000, (n_dec,), generator=g).tolist()
+    ext = [400, 257, 129] + [1] * n_dec
+    run_extend_case(_manual_case(cached, ext, Hq=32, Hkv=8, seed=78))
+
+
 def test_extend_prefix_shared_equals_private():
     """Requests pointing at one set of radix-cache prefix rows give bit-identical
     output to requests holding private copies of the same values."""

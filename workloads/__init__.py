@@ -389,3 +389,49 @@ def extend_positions(batch: ExtendBatch) -> torch.Tensor:
     parts = [torch.arange(int(c), int(c) + int(e), dtype=torch.int32)
              for c, e in zip(batch.cached_lens.tolist(), batch.extend_lens.tolist())]
     return torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int32)
+
+
+# --------------------------------------------------------------------------- #
+# decode with a radix-shared prefix
+# --------------------------------------------------------------------------- #
+def make_shared_prefix_decode_case(name: str, *, num_q_heads: int, num_kv_heads: int,
+                                   head_dim: int, batch: int, prefix_len: int, suffix_lo: int,
+                                   suffix_hi: int, pool_factor: float = 1.2,
+                                   value_std: float = 0.5, seed: int = 0) -> DecodeCase:
+    """Decode step for requests that all matched one cached prefix: the first
+    prefix_len page-table entries of every request are the same physical rows
+    (mini-sglang-learn, radix-cache chapter), followed by a private suffix of
+    U[suffix_lo, suffix_hi] cached tokens and the token stored this step.
+    Rows come from one random permutation of the pool; one layer."""
+    g = torch.Generator().manual_seed(seed)
+    suf = torch.randint(suffix_lo, suffix_hi + 1, (batch,), generator=g).tolist()
+    seq = [prefix_len + s + 1 for s in suf]
+    need = prefix_len + sum(s + 1 for s in suf)
+    live = max(int(math.ceil(pool_factor * need)), need)
+    R = live + 2
+    poison = R - 1
+    perm = torch.randperm(live, generator=g).to(torch.int32)
+    width = align_up(max(seq))
+    pt = torch.full((batch, width), poison, dtype=torch.int32)
+    pt[:, :prefix_len] = perm[:prefix_len]
+    off = prefix_len
+    for r, n in enumerate(seq):
+        k = n - prefix_len
+        pt[r, prefix_len:n] = perm[off:off + k]
+        off += k
+    seq_lens = torch.tensor(seq, dtype=torch.int32)
+    out_loc = torch.tensor([int(pt[r, n - 1]) for r, n in enumerate(seq)], dtype=torch.int32)
+    case = DecodeCase(name=name, num_layers=1, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                      head_dim=head_dim, page_size=1, batch=batch, num_real=batch, num_rows=R,
+                      seq_lens=seq_lens, page_table=pt, out_loc=out_loc,
+                      sm_scale=1.0 / math.sqrt(head_dim), value_std=value_std, seed=seed)
+    case.shared_len = prefix_len  # type: ignore[attr-defined]
+    return case
+
+
+def decode_shared_prefix_qwen3(seed: int = 1005) -> DecodeCase:
+    """Qwen3-0.6B-shaped decode (H_q 16, H_kv 8, d 128) for 64 requests that
+    share a 4096-token cached prefix and add private suffixes of U[16, 512]."""
+    return make_shared_prefix_decode_case("shared-prefix-decode-b64-p4096-s16-512", num_q_heads=16,
+                                          num_kv_heads=8, head_dim=128, batch=64, prefix_len=4096,
+                                          suffix_lo=16, suffix_hi=512, seed=seed)
