@@ -332,6 +332,44 @@ def run_gpu(args, world, rank, local):
     peak = peaks["hbm_gbs"]
     traffic = profile_traffic("decode.cu", "decode_qwen3_0p6b.md")
 
+    # ---- the other decode workloads, one layer each: per-call GB/s and tokens/s ----
+    others = None
+    if not args.no_extend:
+        others = []
+        for oc in (workloads.decode_llama3_8b(num_layers=1), workloads.decode_long_page64()):
+            opool_t, ok_, ov_, oq = workloads.make_decode_values(oc, dev)
+            opool = mk.KVPool(opool_t, oc.page_size)
+            opt, osl, oloc = oc.page_table.to(dev), oc.seq_lens.to(dev), oc.out_loc.to(dev)
+            ows = mk.decode_workspace(oc.batch, oc.num_q_heads, opool)
+            oout = torch.empty_like(oq[0])
+
+            def ostep():
+                mk.minisgl_store_kv(opool, 0, ok_[0], ov_[0], oloc)
+                mk.minisgl_decode_attn(opool, 0, oq[0], opt, osl, oc.sm_scale, out=oout, workspace=ows)
+
+            for _ in range(args.warmup):
+                ostep()
+            torch.cuda.synchronize()
+            oev = []
+            for _ in range(max(10, args.steps // 10)):
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                ostep()
+                b_.record(stream)
+                oev.append((a, b_))
+            torch.cuda.synchronize()
+            oms = statistics.mean(a.elapsed_time(b_) for a, b_ in oev)
+            ob = decode_layer_bytes(oc) + store_layer_bytes(oc)
+            others.append({"workload": oc.name, "batch": oc.batch, "real_requests": oc.num_real,
+                           "H_q": oc.num_q_heads, "H_kv": oc.num_kv_heads, "page_size": oc.page_size,
+                           "context_tokens": int(oc.seq_lens[:oc.num_real].sum()),
+                           "ms_per_layer": round(oms, 5),
+                           "achieved_gbs": round(ob / (oms * 1e-3) / 1e9, 1),
+                           "frac_of_hbm": round(ob / (oms * 1e-3) / 1e9 / peak, 4),
+                           "tokens_per_s_per_layer": round(oc.num_real / (oms * 1e-3), 1),
+                           "l2": "inputs larger than L2 (%.1f GB of K/V per call)" % (ob / 1e9)})
+            del opool_t, ok_, ov_, oq
+
     # ---- shared-prefix (cascade) decode vs plain decode on one radix-shared batch ----
     casc = None
     if not args.no_extend:
@@ -520,6 +558,7 @@ def run_gpu(args, world, rank, local):
         "extend": ext,
         "rope_store_kv": rope,
         "cascade_decode": casc,
+        "decode_other_workloads": others,
         "cpu_baseline": cpu,
     }
     if rank == 0:
