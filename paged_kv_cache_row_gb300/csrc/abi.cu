@@ -9,12 +9,21 @@
 #include <cstdio>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.h"
 #include "minisgl.h"
 
 namespace {
 
 thread_local std::string g_err;
+
+// An NVTX range around each entry point, so a profiler timeline shows the
+// library's calls by name (NVTX does nothing unless a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 int fail(int code, const char *fmt, ...) {
     char buf[512];
@@ -112,6 +121,7 @@ int minisgl_store_kv(const minisgl_kv_pool *pool, int32_t layer, const void *k, 
                      int64_t k_tok_stride, int64_t v_tok_stride, const int32_t *out_loc,
                      int32_t n_tokens, void *stream) {
     g_err.clear();
+    NvtxRange nvtx_range("minisgl_store_kv");
     if (int rc = check_pool(pool, layer, "store_kv")) return rc;
     if (n_tokens < 0) return fail(MINISGL_ERR_ARG, "store_kv: n_tokens < 0");
     if (n_tokens == 0) return MINISGL_OK;
@@ -150,6 +160,7 @@ int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         float sm_scale, void *out, void *workspace, size_t workspace_bytes,
                         int32_t split_tokens, void *stream) {
     g_err.clear();
+    NvtxRange nvtx_range("minisgl_decode_attn");
     if (int rc = check_pool(pool, layer, "decode_attn")) return rc;
     if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "decode_attn")) return rc;
     if (batch < 0 || batch > 4096) return fail(MINISGL_ERR_ARG, "decode_attn: batch %d outside [0, 4096]", batch);
@@ -211,6 +222,7 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         const int32_t *extend_lens, const int32_t *q_offsets,
                         int32_t total_q_tokens, float sm_scale, void *out, void *stream) {
     g_err.clear();
+    NvtxRange nvtx_range("minisgl_extend_attn");
     if (int rc = check_pool(pool, layer, "extend_attn")) return rc;
     if (pool->head_dim != 128)
         return fail(MINISGL_ERR_UNSUPPORTED, "extend_attn: head_dim %d (only 128)", pool->head_dim);
@@ -289,6 +301,7 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
                                 int32_t shared_len, float sm_scale, void *out, void *workspace,
                                 size_t workspace_bytes, void *stream) {
     g_err.clear();
+    NvtxRange nvtx_range("minisgl_cascade_decode_attn");
     if (int rc = check_pool(pool, layer, "cascade_decode_attn")) return rc;
     if (pool->head_dim != 128)
         return fail(MINISGL_ERR_UNSUPPORTED, "cascade_decode_attn: head_dim %d (only 128)", pool->head_dim);
@@ -397,6 +410,7 @@ int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, i
                           int32_t max_positions, const int32_t *out_loc, int32_t n_tokens,
                           void *stream) {
     g_err.clear();
+    NvtxRange nvtx_range("minisgl_rope_store_kv");
     if (int rc = check_pool(pool, layer, "rope_store_kv")) return rc;
     if (num_q_heads < 1) return fail(MINISGL_ERR_ARG, "rope_store_kv: num_q_heads < 1");
     if (n_tokens < 0) return fail(MINISGL_ERR_ARG, "rope_store_kv: n_tokens < 0");
