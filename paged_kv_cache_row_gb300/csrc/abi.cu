@@ -278,6 +278,17 @@ constexpr int CASCADE_SUFFIX_SPLITS = 16;
 // int32 metadata (4 arrays of chunks+1, one of batch), fp32 prefix partials
 // [chunks, B, Hq, D] and their LSEs [chunks, B, Hq], the bf16 suffix result
 // [B, Hq, D] and its LSEs [B, Hq], then a decode workspace for the suffix.
+// Most prefix chunks a call with this shape uses: about two work items per
+// SM (a work item covers 2*128/G query rows of one KV head), at most 32.
+int64_t cascade_chunk_cap(int64_t batch, int64_t hq, int64_t hkv) {
+    const int64_t g = std::max<int64_t>(1, hq / hkv);
+    const int64_t tq2 = std::max<int64_t>(1, 2 * (128 / g));
+    const int64_t items = std::max<int64_t>(1, ((batch + tq2 - 1) / tq2) * hkv);
+    int64_t sms = minisgl::device_sm_count();
+    if (sms <= 0) sms = 1024;  // no device: the 32-chunk ceiling decides
+    return std::max<int64_t>(1, std::min<int64_t>((2 * sms + items - 1) / items, CASCADE_MAX_CHUNKS));
+}
+
 size_t cascade_bytes(int64_t batch, int64_t hq, int64_t hkv, int64_t d, int64_t chunks) {
     return align256((size_t)(4 * (chunks + 1) + batch) * 4) +
            align256((size_t)chunks * batch * hq * d * 4) + align256((size_t)chunks * batch * hq * 4) +
@@ -292,7 +303,8 @@ extern "C" {
 size_t minisgl_cascade_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim) {
     if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1) return 0;
-    return cascade_bytes(batch, num_q_heads, num_kv_heads, head_dim, CASCADE_MAX_CHUNKS);
+    return cascade_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                         cascade_chunk_cap(batch, num_q_heads, num_kv_heads));
 }
 
 int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
@@ -324,10 +336,8 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
         return fail(MINISGL_ERR_SHAPE, "cascade_decode_attn: q, out 16-byte and workspace 256-byte aligned");
     // prefix chunks: about two work items per SM, at least four 128-token tiles each
     const int64_t tiles = (shared_len + 127) / 128;
-    const int64_t tq2 = 2 * (128 / G);
-    const int64_t items_per_chunk = ((batch + tq2 - 1) / tq2) * pool->num_kv_heads;
-    int64_t chunks = (2 * (int64_t)minisgl::device_sm_count() + items_per_chunk - 1) / items_per_chunk;
-    chunks = std::max<int64_t>(1, std::min<int64_t>({chunks, (tiles + 3) / 4, (int64_t)CASCADE_MAX_CHUNKS}));
+    int64_t chunks = cascade_chunk_cap(batch, num_q_heads, pool->num_kv_heads);
+    chunks = std::max<int64_t>(1, std::min<int64_t>(chunks, (tiles + 3) / 4));
     const int64_t chunk_len = ((tiles + chunks - 1) / chunks) * 128;
     chunks = (shared_len + chunk_len - 1) / chunk_len;
     const int64_t Hkv = pool->num_kv_heads, d = pool->head_dim;
