@@ -180,15 +180,22 @@ def profile_traffic(kernel_file: str, summary_name: str):
 # --------------------------------------------------------------------------- #
 # distributed plumbing
 # --------------------------------------------------------------------------- #
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, backend: str = ""):
+    """Rank setup from the torchrun environment.  One process per GPU with
+    NCCL on a GPU machine; the gloo backend (CPU) serves the multi-process tests.
+    The data path has no collective: every rank runs its own batch."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -200,12 +207,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: the job finishes when every rank has."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed (each rank the same
+    amount: weak scaling) over the slowest rank's time, per second."""
+    return world * units_per_rank / (ms_max * 1e-3)
 
 
 # --------------------------------------------------------------------------- #
@@ -308,8 +323,8 @@ def run_gpu(args, world, rank, local):
     dec_b = decode_layer_bytes(case)
     st_b = store_layer_bytes(case)
     step_bytes = L * (dec_b + st_b)
-    value = world * step_bytes / (ms * 1e-3) / 1e9
-    tokens_s = world * case.num_real / (ms * 1e-3)
+    value = job_rate(step_bytes, world, ms) / 1e9
+    tokens_s = job_rate(case.num_real, world, ms)
 
     # ---- per-call durations of the dominant call, CUDA events on the launch stream ----
     n_rep = max(3, min(args.steps, 50))
@@ -436,7 +451,7 @@ def run_gpu(args, world, rank, local):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world)
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_value = job_rate(step_bytes, world, e2e_ms) / 1e9
 
     # ---- extend: radix-shared chunked prefill, store_kv + extend per batch ----
     ext = None
