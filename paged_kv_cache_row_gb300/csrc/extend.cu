@@ -31,7 +31,14 @@
 //     P = 2^(s - m) as bf16 back into the upper 64 columns of its S row, where
 //     the PV MMA reads it.  O_X is rescaled in tensor memory only
 //     when the max has grown by more than 2^8 (the final O / l does not
-//     depend on when the rescale happens).  Epilogue: O / l -> bf16 -> global.
+//     depend on when the rescale happens).  After a query tile's first K/V
+//     tile, full (unmasked) tiles skip the max pass: exponentials use the
+//     running max m, P stays in registers, and only if the tile's sum shows a
+//     score more than 2^20 above m (or a NaN) does the row, still intact in
+//     tensor memory, go through the exact max-then-exponentiate path.  Every
+//     P is then at most 2^20, well inside fp32 and bf16 range, and bf16
+//     keeps the same relative precision at any magnitude.
+//     Epilogue: O / l -> bf16 -> global.
 //   * Tensor memory (512 columns): S_A 0-127, S_B 128-255, O_A 256-383,
 //     O_B 384-511.  Shared memory: Q_A, Q_B (32 KB each), two K/V stages
 //     (64 KB each).
@@ -168,6 +175,26 @@ __device__ __forceinline__ void quarter_softmax(const uint32_t (&q)[32], bool fu
         pw[e] = pack_bf16x2(p0, p1);
     }
     tmem_st16(dst, pw);
+}
+
+// 2^(s*scale - m) for the 64 scores of a full half row: 32 bf16 pairs into pw,
+// sums into the packed accumulator lt
+__device__ __forceinline__ void exp_half(const uint32_t (&h)[64], uint64_t scale2, uint64_t negm2,
+                                         uint64_t &lt, uint32_t (&pw)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        float x0, x1;
+        f2split(ffma2(f2(__uint_as_float(h[2 * e]), __uint_as_float(h[2 * e + 1])), scale2, negm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        lt = fadd2(lt, f2(p0, p1));
+        pw[e] = pack_bf16x2(p0, p1);
+    }
+}
+__device__ __forceinline__ void tmem_st16_from(uint32_t dst, const uint32_t (&pw)[32], int base) {
+    uint32_t q[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) q[k] = pw[base + k];
+    tmem_st16(dst, q);
 }
 
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
@@ -513,6 +540,42 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const int rel = lim - j * ROWS;  // last visible column of this tile
                     const bool full = rel >= ROWS - 1;
+                    if (j > 0 && __all_sync(0xffffffffu, full)) {
+                        // Running-max fast path: exponentials with the max m of the
+                        // earlier tiles, no max pass.  P stays in registers until the
+                        // tile's sum shows no score exceeded m by more than 20 (base
+                        // 2); otherwise (or on NaN) the S row, still intact, goes
+                        // through the exact path below.
+                        const uint64_t negm2 = f2(-m, -m);
+                        uint32_t p0[32], p1[32];
+                        uint64_t lt = f2(0.f, 0.f);
+                        {
+                            uint32_t h[64];
+                            tmem_ld64(scol, h);
+                            tmem_wait_ld();
+                            exp_half(h, scale2, negm2, lt, p0);
+                        }
+                        {
+                            uint32_t h[64];
+                            tmem_ld64(scol + 64, h);
+                            tmem_wait_ld();
+                            exp_half(h, scale2, negm2, lt, p1);
+                        }
+                        float ta, tb;
+                        f2split(lt, ta, tb);
+                        const float ts = ta + tb;
+                        if (!__any_sync(0xffffffffu, !(ts <= 1048576.f))) {
+                            tmem_st16_from(scol + 64, p0, 0);
+                            tmem_st16_from(scol + 80, p0, 16);
+                            tmem_st16_from(scol + 96, p1, 0);
+                            tmem_st16_from(scol + 112, p1, 16);
+                            l2 = fadd2(l2, lt);
+                            tmem_wait_st();
+                            tc_fence_before();
+                            mbar_arrive(p_full(x));
+                            continue;
+                        }
+                    }
                     // pass 1: max of the raw scores (sm_scale > 0); the last 32
                     // columns stay in registers for pass 2
                     uint32_t top[32];

@@ -101,6 +101,42 @@ def test_extend_mixed_chunk_and_decode_batch():
     run_extend_case(_manual_case(cached, ext, Hq=32, Hkv=8, seed=78))
 
 
+def test_extend_growing_scores_take_the_exact_path():
+    """Scores that jump by far more than the rescale threshold from one
+    128-token K/V tile to the next: the running-max fast path must hand such
+    tiles to the exact path (and rescale O); results still match the oracle."""
+    case = _manual_case([600, 0], [80, 300], Hq=8, Hkv=2, seed=12)
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    b = case.batches[0]
+    k, v, q = per_batch[0]
+    g = torch.Generator(device=DEV).manual_seed(3)
+    levels = torch.tensor([0.05, 0.6, 1.6, 3.4, 6.0], device=DEV)
+
+    def keys(pos):  # key value grows with the position's 128-token tile
+        f = levels[(pos // 128).clamp(max=4)]
+        noise = torch.randn((pos.numel(), 2, 128), generator=g, device=DEV) * 0.02
+        return (f[:, None, None] + noise).to(torch.bfloat16)
+
+    for r, (C, E) in enumerate(zip(b.cached_lens.tolist(), b.extend_lens.tolist())):
+        o = int(b.q_offsets[r])
+        if C:
+            rows = b.page_table[r, :C].long().to(DEV)
+            pool_t[0, 0, rows] = keys(torch.arange(C, device=DEV))
+        k[o:o + E] = keys(torch.arange(C, C + E, device=DEV))
+    q.copy_((0.5 + 0.05 * torch.randn(q.shape, generator=g, device=DEV)).to(torch.bfloat16))
+    hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+    pool = mk.KVPool(pool_t)
+    mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+    o = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                               b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+    torch.cuda.synchronize()
+    orc = oracle.get()
+    orc.store_kv(hk, hv, k.cpu(), v.cpu(), b.out_loc)
+    ref = orc.extend(q.cpu(), hk, hv, b.page_table, b.cached_lens, b.extend_lens, case.sm_scale)
+    gu.check_attn(o, ref, "growing scores")
+    assert mk.minisgl_debug_timeout_count() == 0
+
+
 def test_extend_prefix_shared_equals_private():
     """Requests pointing at one set of radix-cache prefix rows give bit-identical
     output to requests holding private copies of the same values."""
