@@ -104,6 +104,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int cc) {
 // Bounded mbarrier wait shared by all roles: once one wait has run out, the
 // CTA stops waiting altogether so every thread reaches the end quickly.
 __device__ __forceinline__ void guarded_wait(uint32_t b, uint32_t parity, int *abort_flag) {
+    if (mbar_test_wait(b, parity)) return;
     if (*((volatile int *)abort_flag)) return;
     if (!mbar_wait(b, parity, WAIT_LIMIT)) {
         *((volatile int *)abort_flag) = 1;
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t dv0 = smem_desc_sw128(sKV + TILE_BYTES, HALF, 1024);
             const uint64_t dv1 = smem_desc_sw128(sKV + 3 * TILE_BYTES, HALF, 1024);
             auto mwait = [&](uint32_t b, uint32_t par) {
-                if (!mbar_try_wait(b, par)) wait(b, par);
+                if (!mbar_test_wait(b, par)) wait(b, par);
             };
             uint32_t kv_iter = 0, cnt_a = 0, cnt_b = 0;
             for (uint32_t n = 0;; ++n) {
