@@ -6,6 +6,7 @@
  *
  *   minisgl_store_kv     scatter this step's new K/V token rows into the pool
  *   minisgl_decode_attn  one query token per request, split-KV, then an LSE merge
+ *   minisgl_store_decode_attn  store_kv and decode in one pass
  *   minisgl_extend_attn  causal attention for the new tokens of chunked prefill
  *   minisgl_rope_store_kv  rotary position embedding of q and k fused with store_kv
  *   minisgl_cascade_decode_attn  decode for requests sharing a prefix, prefix read once
@@ -157,6 +158,27 @@ int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
                         float sm_scale, void *out, void *workspace, size_t workspace_bytes,
                         int32_t split_tokens, void *stream);
+
+/*
+ * store_kv fused into decode [learn, paged KV pool: each layer stores the
+ * step's new K/V rows, then attends].  Same results as minisgl_store_kv of
+ * (k, v, out_loc) followed by minisgl_decode_attn with the remaining
+ * arguments, in one kernel pass: the warp that reads a request's last tile
+ * writes the request's new K/V rows (one per request: k[r], v[r], token
+ * strides in elements) to row out_loc[r], and positions whose page-table row
+ * is the request's out_loc row read the new rows directly.  Conditions (the
+ * decode step satisfies them): every seq_lens[r] >= 1, and no request reads
+ * another request's out_loc row unless both store identical values there
+ * (CUDA-Graph padding requests sharing the dummy row).  Rows of requests
+ * with seq_lens[r] == 0 are not stored.
+ */
+int minisgl_store_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *k,
+                              const void *v, int64_t k_tok_stride, int64_t v_tok_stride,
+                              const int32_t *out_loc, const void *q, int32_t num_q_heads,
+                              const int32_t *page_table, int32_t batch, int64_t pt_row_stride,
+                              int32_t pt_width, const int32_t *seq_lens, float sm_scale, void *out,
+                              void *workspace, size_t workspace_bytes, int32_t split_tokens,
+                              void *stream);
 
 /*
  * Extend (chunked-prefill) attention [learn: request-state passage

@@ -26,14 +26,14 @@ __all__ = [
     "minisgl_decode_workspace_bytes", "minisgl_device_sm_count", "minisgl_debug_timeout_count",
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
     "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv", "minisgl_cascade_decode_attn",
-    "minisgl_cascade_workspace_bytes",
+    "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
 ]
 
 EXPORTED_SYMBOLS = [
     "minisgl_store_kv", "minisgl_decode_workspace_bytes", "minisgl_decode_attn",
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
     "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
-    "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes",
+    "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
 ]
 
 MINISGL_BF16 = 1
@@ -85,6 +85,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_cascade_decode_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, i32, f32, vp,
                                                 vp, sz, vp]
     lib.minisgl_cascade_decode_attn.restype = ctypes.c_int
+    lib.minisgl_store_decode_attn.argtypes = [P, i32, vp, vp, i64, i64, vp, vp, i32, vp, i32, i64, i32,
+                                              vp, f32, vp, vp, sz, i32, vp]
+    lib.minisgl_store_decode_attn.restype = ctypes.c_int
     lib.minisgl_last_error.argtypes = []
     lib.minisgl_last_error.restype = ctypes.c_char_p
     lib.minisgl_device_sm_count.argtypes = []
@@ -359,4 +362,42 @@ def minisgl_cascade_decode_attn(pool: KVPool, layer: int, q: torch.Tensor, page_
                                            B, page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
                                            int(shared_len), float(sm_scale), _ptr(out), _ptr(workspace),
                                            workspace.numel(), _stream(stream)), "cascade_decode_attn")
+    return out
+
+
+def minisgl_store_decode_attn(pool: KVPool, layer: int, k: torch.Tensor, v: torch.Tensor,
+                              out_loc: torch.Tensor, q: torch.Tensor, page_table: torch.Tensor,
+                              seq_lens: torch.Tensor, sm_scale: float,
+                              out: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None, split_tokens: int = 0,
+                              max_splits: int = 16, stream=None) -> torch.Tensor:
+    """minisgl_store_kv(k, v, out_loc) and minisgl_decode_attn in one pass
+    (k, v: [B, H_kv, d], one new row per request)."""
+    lib = load_library()
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nm, torch.bfloat16)
+    for t, nm in ((page_table, "page_table"), (seq_lens, "seq_lens"), (out_loc, "out_loc")):
+        _need(t, nm, torch.int32)
+    B, Hq, d = q.shape
+    if not q.is_contiguous() or d != pool.head_dim:
+        raise MinisglError("q must be contiguous [B, H_q, head_dim]")
+    row = pool.num_kv_heads * d
+    for t, nm in ((k, "k"), (v, "v")):
+        if t.shape[0] != B or t[0].numel() != row or not t[0].is_contiguous():
+            raise MinisglError(f"{nm} must be [B, H_kv, d] with contiguous rows")
+    if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if seq_lens.numel() != B or not seq_lens.is_contiguous() or out_loc.numel() != B \
+            or not out_loc.is_contiguous():
+        raise MinisglError("seq_lens and out_loc must be contiguous [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, pool, max_splits)
+    _check(lib.minisgl_store_decode_attn(ctypes.byref(pool.desc), layer, _ptr(k), _ptr(v), k.stride(0),
+                                         v.stride(0), _ptr(out_loc), _ptr(q), Hq, _ptr(page_table), B,
+                                         page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
+                                         float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                         split_tokens, _stream(stream)), "store_decode_attn")
     return out

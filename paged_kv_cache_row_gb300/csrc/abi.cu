@@ -154,13 +154,21 @@ size_t minisgl_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_
     return ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_splits);
 }
 
-int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
-                        int32_t num_q_heads, const int32_t *page_table, int32_t batch,
-                        int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
-                        float sm_scale, void *out, void *workspace, size_t workspace_bytes,
-                        int32_t split_tokens, void *stream) {
-    g_err.clear();
-    NvtxRange nvtx_range("minisgl_decode_attn");
+}  // extern "C"
+
+namespace {
+
+// The new K/V rows of minisgl_store_decode_attn (null for plain decode).
+struct FusedStore {
+    const void *k, *v;
+    int64_t k_tok_stride, v_tok_stride;
+    const int32_t *out_loc;
+};
+
+int decode_impl(const minisgl_kv_pool *pool, int32_t layer, const void *q, int32_t num_q_heads,
+                const int32_t *page_table, int32_t batch, int64_t pt_row_stride, int32_t pt_width,
+                const int32_t *seq_lens, float sm_scale, void *out, void *workspace,
+                size_t workspace_bytes, int32_t split_tokens, void *stream, const FusedStore *fs) {
     if (int rc = check_pool(pool, layer, "decode_attn")) return rc;
     if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "decode_attn")) return rc;
     if (batch < 0 || batch > 4096) return fail(MINISGL_ERR_ARG, "decode_attn: batch %d outside [0, 4096]", batch);
@@ -213,7 +221,52 @@ int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
     a.max_splits = splits;
     a.split_tokens = split_tokens;
     a.lse_out = nullptr;
+    a.out_loc = fs ? fs->out_loc : nullptr;
+    a.k_new = fs ? fs->k : nullptr;
+    a.v_new = fs ? fs->v : nullptr;
+    a.new_k_stride = fs ? fs->k_tok_stride : 0;
+    a.new_v_stride = fs ? fs->v_tok_stride : 0;
     return cuda_status(minisgl::launch_decode(a, static_cast<cudaStream_t>(stream)), "decode_attn");
+}
+
+}  // namespace
+
+extern "C" {
+
+int minisgl_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                        int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                        int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
+                        float sm_scale, void *out, void *workspace, size_t workspace_bytes,
+                        int32_t split_tokens, void *stream) {
+    g_err.clear();
+    NvtxRange nvtx_range("minisgl_decode_attn");
+    return decode_impl(pool, layer, q, num_q_heads, page_table, batch, pt_row_stride, pt_width,
+                       seq_lens, sm_scale, out, workspace, workspace_bytes, split_tokens, stream,
+                       nullptr);
+}
+
+int minisgl_store_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *k,
+                              const void *v, int64_t k_tok_stride, int64_t v_tok_stride,
+                              const int32_t *out_loc, const void *q, int32_t num_q_heads,
+                              const int32_t *page_table, int32_t batch, int64_t pt_row_stride,
+                              int32_t pt_width, const int32_t *seq_lens, float sm_scale, void *out,
+                              void *workspace, size_t workspace_bytes, int32_t split_tokens,
+                              void *stream) {
+    g_err.clear();
+    NvtxRange nvtx_range("minisgl_store_decode_attn");
+    if (int rc = check_pool(pool, layer, "store_decode_attn")) return rc;
+    if (batch > 0) {
+        if (!k || !v || !out_loc) return fail(MINISGL_ERR_ARG, "store_decode_attn: NULL k, v or out_loc");
+        const int64_t row = (int64_t)pool->num_kv_heads * pool->head_dim;
+        if (!aligned16(k) || !aligned16(v))
+            return fail(MINISGL_ERR_SHAPE, "store_decode_attn: k and v must be 16-byte aligned");
+        if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+            return fail(MINISGL_ERR_SHAPE,
+                        "store_decode_attn: token strides must be >= H_kv*d and multiples of 8");
+    }
+    const FusedStore fs{k, v, k_tok_stride, v_tok_stride, out_loc};
+    return decode_impl(pool, layer, q, num_q_heads, page_table, batch, pt_row_stride, pt_width,
+                       seq_lens, sm_scale, out, workspace, workspace_bytes, split_tokens, stream, &fs);
 }
 
 int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
@@ -410,6 +463,9 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
     sd.max_splits = CASCADE_SUFFIX_SPLITS;
     sd.split_tokens = 0;
     sd.lse_out = c.suf_lse;
+    sd.out_loc = nullptr;
+    sd.k_new = sd.v_new = nullptr;
+    sd.new_k_stride = sd.new_v_stride = 0;
     return cuda_status(minisgl::launch_cascade(c, base, static_cast<cudaStream_t>(stream)),
                        "cascade_decode_attn");
 }

@@ -152,12 +152,15 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
             }
         }
     };
-    // lane < 16: physical row of token 16*j + lane of the cursor's request, or -1 past its end
+    // lane < 16: physical row of token 16*j + lane of the cursor's request, or -1 past its
+    // end; with the fused store, -2 for a position whose row is the request's out_loc row
+    // (its K/V are read from this step's new rows, which this kernel is storing there)
     auto load_rows = [&](const Cursor &c) -> int {
         const int tok = c.j * TILE + lane;
         if (lane >= TILE || tok >= c.n) return -1;
-        const int row = __ldg(a.page_table + (int64_t)c.r * a.pt_stride + tok);
-        return min(max(row, 0), a.num_rows - 1);
+        const int row = min(max(__ldg(a.page_table + (int64_t)c.r * a.pt_stride + tok), 0), a.num_rows - 1);
+        if (a.out_loc && row == min(max(__ldg(a.out_loc + c.r), 0), a.num_rows - 1)) return -2;
+        return row;
     };
     // K and V rows of one tile (plus the group's queries when the tile opens a stream)
     auto issue = [&](int stage, const Cursor &c, int rows, bool with_q) {
@@ -170,9 +173,30 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
             const int row = __shfl_sync(0xffffffffu, rows, tt);
             const uint32_t off = swz(tt, cc, C::RB);
             const int64_t e = (int64_t)max(row, 0) * a.row_stride + head + cc * 8;
-            const int bytes = row >= 0 ? 16 : 0;
-            cp_async_16(st + off, Kl + e, bytes);
-            cp_async_16(st + C::KV_BYTES + off, Vl + e, bytes);
+            const int bytes = row != -1 ? 16 : 0;
+            const __nv_bfloat16 *ks = Kl + e, *vs = Vl + e;
+            if (row == -2) {
+                ks = static_cast<const __nv_bfloat16 *>(a.k_new) + (int64_t)c.r * a.new_k_stride + head + cc * 8;
+                vs = static_cast<const __nv_bfloat16 *>(a.v_new) + (int64_t)c.r * a.new_v_stride + head + cc * 8;
+            }
+            cp_async_16(st + off, ks, bytes);
+            cp_async_16(st + C::KV_BYTES + off, vs, bytes);
+        }
+        if (a.out_loc && c.j == c.nt - 1) {
+            // fused store_kv: the warp that reads a stream's last tile writes the
+            // request's new K and V head slice to its out_loc row (lane < CPR: K
+            // chunk, else V chunk)
+            const int row = min(max(__ldg(a.out_loc + c.r), 0), a.num_rows - 1);
+            for (int ch = lane; ch < 2 * C::CPR; ch += 32) {
+                const bool isv = ch >= C::CPR;
+                const int cc = isv ? ch - C::CPR : ch;
+                const __nv_bfloat16 *src =
+                    static_cast<const __nv_bfloat16 *>(isv ? a.v_new : a.k_new) +
+                    (int64_t)c.r * (isv ? a.new_v_stride : a.new_k_stride) + head + cc * 8;
+                __nv_bfloat16 *dst = const_cast<__nv_bfloat16 *>(isv ? Vl : Kl) +
+                                     (int64_t)row * a.row_stride + head + cc * 8;
+                st_v4(dst, ld_nc_v4(src));
+            }
         }
         if (with_q) {
             const __nv_bfloat16 *src = Q + ((int64_t)c.r * Hq + c.g * G) * D;

@@ -55,6 +55,11 @@ struct DecodeArgs {
     int32_t max_splits;
     int32_t split_tokens;         // 0 = automatic
     float *lse_out;               // optional [B, Hq] natural-log LSE of each output row
+    // optional fused store_kv: request r's new K/V rows (k_new + r*new_k_stride,
+    // v_new + r*new_v_stride) go to pool row out_loc[r]; null out_loc = no store
+    const int32_t *out_loc;
+    const void *k_new, *v_new;
+    int64_t new_k_stride, new_v_stride;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 

@@ -30,8 +30,9 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def run_case(case, split_tokens=0, max_splits=16, layers=None):
-    """Store + decode every layer; compare pool bytes and outputs with the oracle."""
+def run_case(case, split_tokens=0, max_splits=16, layers=None, fused=False):
+    """Store + decode every layer (fused: in one minisgl_store_decode_attn
+    call); compare pool bytes and outputs with the oracle."""
     pool_t, k_new, v_new, q = workloads.make_decode_values(case, DEV)
     host_pool = [(gu.u16(pool_t[0, l]), gu.u16(pool_t[1, l])) for l in range(case.num_layers)]
     pool = mk.KVPool(pool_t, case.page_size)
@@ -39,9 +40,14 @@ def run_case(case, split_tokens=0, max_splits=16, layers=None):
     orc = oracle.get()
     outs = []
     for l in (layers or range(case.num_layers)):
-        mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
-        o = mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, split_tokens=split_tokens,
-                                   max_splits=max_splits)
+        if fused:
+            o = mk.minisgl_store_decode_attn(pool, l, k_new[l], v_new[l], loc, q[l], pt, sl,
+                                             case.sm_scale, split_tokens=split_tokens,
+                                             max_splits=max_splits)
+        else:
+            mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
+            o = mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale,
+                                       split_tokens=split_tokens, max_splits=max_splits)
         torch.cuda.synchronize()
         hk, hv = host_pool[l]
         orc.store_kv(hk, hv, k_new[l].cpu(), v_new[l].cpu(), case.out_loc)
@@ -73,6 +79,26 @@ def test_decode_small(name, Hq, Hkv, d, page, B, lo, hi, dummies, L):
                                       num_dummy=dummies, dummy_seq_len=9, min_rows=256,
                                       value_std=0.5, seed=zlib.crc32(name.encode()) % 10000)
     run_case(case)
+
+
+@pytest.mark.parametrize("name,Hq,Hkv,d,page,B,lo,hi,dummies,L", SMALL, ids=[s[0] for s in SMALL])
+def test_store_decode_fused_small(name, Hq, Hkv, d, page, B, lo, hi, dummies, L):
+    """store_kv fused into decode: the same pool bytes and outputs as the
+    two calls, on every small case (padding requests with 9-token contexts on
+    the dummy row included)."""
+    case = workloads.make_decode_case(name, num_layers=L, num_q_heads=Hq, num_kv_heads=Hkv,
+                                      head_dim=d, page_size=page, batch=B, ctx_lo=lo, ctx_hi=hi,
+                                      num_dummy=dummies, dummy_seq_len=9, min_rows=256,
+                                      value_std=0.5, seed=zlib.crc32(name.encode()) % 10000)
+    run_case(case, fused=True)
+
+
+@pytest.mark.parametrize("split_tokens", [16, 48])
+def test_store_decode_fused_split_counts(split_tokens):
+    case = workloads.make_decode_case("fused-splits", num_layers=1, num_q_heads=16, num_kv_heads=4,
+                                      head_dim=128, page_size=1, batch=5, ctx_lo=1, ctx_hi=400,
+                                      value_std=0.5, seed=78)
+    run_case(case, split_tokens=split_tokens, max_splits=64, fused=True)
 
 
 def test_tiny_decode_config():

@@ -24,7 +24,7 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def run_decode_full(case, sample_reqs, sample_layers):
+def run_decode_full(case, sample_reqs, sample_layers, fused=False):
     pool_t, k_new, v_new, q = workloads.make_decode_values(case, DEV)
     pool = mk.KVPool(pool_t, case.page_size)
     pt, sl, loc = case.page_table.to(DEV), case.seq_lens.to(DEV), case.out_loc.to(DEV)
@@ -36,8 +36,12 @@ def run_decode_full(case, sample_reqs, sample_layers):
     ws = mk.decode_workspace(case.batch, case.num_q_heads, pool)
     outs = {}
     for l in range(case.num_layers):  # the whole step, as the benchmark runs it
-        mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
-        o = mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, workspace=ws)
+        if fused:
+            o = mk.minisgl_store_decode_attn(pool, l, k_new[l], v_new[l], loc, q[l], pt, sl,
+                                             case.sm_scale, workspace=ws)
+        else:
+            mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
+            o = mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, workspace=ws)
         if l in sample_layers:
             outs[l] = o.clone()
     torch.cuda.synchronize()
@@ -65,6 +69,12 @@ def test_full_tiny_decode():
 def test_full_qwen3_0p6b_decode():
     case = workloads.decode_qwen3_0p6b()
     run_decode_full(case, [0, 9, 31, 47, 63], [0, case.num_layers - 1])
+
+
+def test_full_qwen3_0p6b_decode_fused_store():
+    """The benchmark's step: store_kv fused into decode, all 28 layers."""
+    case = workloads.decode_qwen3_0p6b()
+    run_decode_full(case, [0, 9, 31, 47, 63], [0, case.num_layers - 1], fused=True)
 
 
 def test_full_llama3_8b_decode_with_padding():
