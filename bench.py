@@ -381,27 +381,37 @@ def run_gpu(args, world, rank, local):
             ows = mk.decode_workspace(oc.batch, oc.num_q_heads, opool)
             oout = torch.empty_like(oq[0])
 
-            def ostep():
+            def ostep_fused():
+                mk.minisgl_store_decode_attn(opool, 0, ok_[0], ov_[0], oloc, oq[0], opt, osl, oc.sm_scale,
+                                             out=oout, workspace=ows)
+
+            def ostep_two():
                 mk.minisgl_store_kv(opool, 0, ok_[0], ov_[0], oloc)
                 mk.minisgl_decode_attn(opool, 0, oq[0], opt, osl, oc.sm_scale, out=oout, workspace=ows)
 
-            for _ in range(args.warmup):
-                ostep()
-            torch.cuda.synchronize()
-            oev = []
-            for _ in range(max(10, args.steps // 10)):
-                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                ostep()
-                b_.record(stream)
-                oev.append((a, b_))
-            torch.cuda.synchronize()
-            oms = statistics.mean(a.elapsed_time(b_) for a, b_ in oev)
+            def otime(fn):
+                for _ in range(args.warmup):
+                    fn()
+                torch.cuda.synchronize()
+                oev = []
+                for _ in range(max(10, args.steps // 10)):
+                    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b_.record(stream)
+                    oev.append((a, b_))
+                torch.cuda.synchronize()
+                return statistics.mean(a.elapsed_time(b_) for a, b_ in oev)
+
+            oms = otime(ostep_fused)
+            oms_two = otime(ostep_two)
             ob = decode_layer_bytes(oc) + store_layer_bytes(oc)
             others.append({"workload": oc.name, "batch": oc.batch, "real_requests": oc.num_real,
                            "H_q": oc.num_q_heads, "H_kv": oc.num_kv_heads, "page_size": oc.page_size,
                            "context_tokens": int(oc.seq_lens[:oc.num_real].sum()),
+                           "call": "minisgl_store_decode_attn",
                            "ms_per_layer": round(oms, 5),
+                           "two_call_ms_per_layer": round(oms_two, 5),
                            "achieved_gbs": round(ob / (oms * 1e-3) / 1e9, 1),
                            "frac_of_hbm": round(ob / (oms * 1e-3) / 1e9 / peak, 4),
                            "tokens_per_s_per_layer": round(oc.num_real / (oms * 1e-3), 1),
