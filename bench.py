@@ -273,6 +273,31 @@ def cpu_cores_used() -> int:
     return 1  # the oracle is single-threaded C
 
 
+def oracle_all_cores(case, pool_t, k_new, v_new, q, budget_s=10.0):
+    """The same oracle on every host core: the batch's requests are dealt
+    round-robin to one thread per core, each thread calling the oracle on its
+    own requests (ctypes releases the GIL, so the C calls run in parallel).
+    Returns (GB/s, threads, sample text)."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores = len(os.sched_getaffinity(0))
+    B = case.batch
+    groups = [list(range(i, B, cores)) for i in range(min(cores, B))]
+    runs = [oracle_decode_sample(case, pool_t, k_new, v_new, q, [0], g) for g in groups]
+    nbytes = sum(b for _, b in runs)
+    with ThreadPoolExecutor(len(runs)) as ex:
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            list(ex.map(lambda rb: rb[0](), runs))
+            n += 1
+            if time.perf_counter() - t0 > budget_s or n >= 200:
+                break
+        dt = time.perf_counter() - t0
+    sample = (f"store_kv + decode of all {B} requests on layer 0, one thread per core "
+              f"({len(runs)} threads), repeated {n}x, {dt:.1f} s, fp64 C")
+    return nbytes * n / dt / 1e9, len(runs), sample
+
+
 # --------------------------------------------------------------------------- #
 # GPU arm
 # --------------------------------------------------------------------------- #
@@ -578,6 +603,9 @@ def run_gpu(args, world, rank, local):
                "kind": "oracle",
                "sample": f"store_kv + decode of requests {reqs} (of {B}) on layer 0, "
                          f"repeated {n}x, {dt:.1f} s, single-threaded fp64 C"}
+        ac_v, ac_threads, ac_sample = oracle_all_cores(case, pool_t, k_new, v_new, q)
+        cpu["all_cores"] = {"value": round(ac_v, 4), "unit": "GB/s", "cores": ac_threads,
+                            "kind": "oracle", "sample": ac_sample}
 
     gpu_launches = args.steps * L * 2  # per layer: decode partial (with the store) + LSE merge
     line = {
