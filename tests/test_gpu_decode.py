@@ -279,3 +279,14 @@ def test_store_kv_strided_and_pagefirst():
     assert torch.equal(pool_t[1, 1].cpu()[loc.long()], v.cpu())
     for l in (0, 2):
         assert np.array_equal(gu.u16(pool_t[0, l].contiguous()), before[l]), "other layers must not change"
+
+
+@pytest.mark.parametrize("split_tokens", [0, 16])
+def test_large_batch_short_contexts(split_tokens):
+    """1040 requests x 8 KV heads = 8320 (request, KV head) streams of at most
+    4 tiles: many streams per warp at the automatic split, and with forced
+    16-token splits nearly every stream is split and merged."""
+    case = workloads.make_decode_case("many-streams", num_layers=1, num_q_heads=8, num_kv_heads=8,
+                                      head_dim=64, page_size=1, batch=1040, ctx_lo=1, ctx_hi=60,
+                                      value_std=0.5, seed=81)
+    run_case(case, split_tokens=split_tokens, max_splits=16)
