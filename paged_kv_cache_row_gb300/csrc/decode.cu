@@ -162,6 +162,16 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
         if (a.out_loc && row == min(max(__ldg(a.out_loc + c.r), 0), a.num_rows - 1)) return -2;
         return row;
     };
+    // fused store_kv: this lane's 16-byte chunk of a new K/V head slice, loaded
+    // when the stream's last tile is issued and written one tile later, so the
+    // load's latency hides behind the tile being computed
+    static_assert(2 * C::CPR <= 32, "one chunk of the new K and V head slice per lane");
+    uint4 st_val = make_uint4(0u, 0u, 0u, 0u);
+    __nv_bfloat16 *st_dst = nullptr;
+    auto store_pending = [&]() {
+        if (st_dst) st_v4(st_dst, st_val);
+        st_dst = nullptr;
+    };
     // K and V rows of one tile (plus the group's queries when the tile opens a stream)
     auto issue = [&](int stage, const Cursor &c, int rows, bool with_q) {
         const uint32_t st = ring + stage * stage_bytes;
@@ -186,16 +196,17 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
             // fused store_kv: the warp that reads a stream's last tile writes the
             // request's new K and V head slice to its out_loc row (lane < CPR: K
             // chunk, else V chunk)
+            store_pending();
             const int row = min(max(__ldg(a.out_loc + c.r), 0), a.num_rows - 1);
-            for (int ch = lane; ch < 2 * C::CPR; ch += 32) {
-                const bool isv = ch >= C::CPR;
-                const int cc = isv ? ch - C::CPR : ch;
+            if (lane < 2 * C::CPR) {
+                const bool isv = lane >= C::CPR;
+                const int cc = isv ? lane - C::CPR : lane;
                 const __nv_bfloat16 *src =
                     static_cast<const __nv_bfloat16 *>(isv ? a.v_new : a.k_new) +
                     (int64_t)c.r * (isv ? a.new_v_stride : a.new_k_stride) + head + cc * 8;
-                __nv_bfloat16 *dst = const_cast<__nv_bfloat16 *>(isv ? Vl : Kl) +
-                                     (int64_t)row * a.row_stride + head + cc * 8;
-                st_v4(dst, ld_nc_v4(src));
+                st_val = ld_nc_v4(src);
+                st_dst = const_cast<__nv_bfloat16 *>(isv ? Vl : Kl) + (int64_t)row * a.row_stride +
+                         head + cc * 8;
             }
         }
         if (with_q) {
@@ -391,8 +402,10 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
             }
             last_j = cc.j;
             if (t + 1 < t1) advance(cc);
+            store_pending();
             __syncwarp();
         }
+        store_pending();
         if (cur_r >= 0) flush();
         cp_async_wait<0>();
         __syncwarp();
