@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     constexpr int CPL = D / 32;  // channels per lane
+    constexpr int PRE = 8;       // partial rows loaded before the weights are known
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     pdl_wait();
@@ -426,32 +427,56 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     if (wid >= a.batch * Hq) return;
     const int r = wid / Hq, h = wid - r * Hq, g = h / G;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (int64_t)wid * D + lane * CPL;
+    // two dependent rounds of loads: the context length and split count, then
+    // the first 32 LSEs together with the first PRE partial rows
     const int n = min(max(__ldg(a.seq_lens + r), 0), a.pt_width);
+    const int cnt = a.split_count[(int64_t)r * Hkv + g];
     if (n == 0) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) out[c] = __float2bfloat16_rn(0.f);
         if (a.lse_out && lane == 0) a.lse_out[wid] = -INFINITY;
         return;
     }
-    const int S = min(a.split_count[(int64_t)r * Hkv + g], a.max_splits);
+    const int S = min(cnt, a.max_splits);
     if (S <= 1) return;
     const int64_t base = (int64_t)wid * a.max_splits;
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < S; s0 += 32)
+    const float *orow = a.ws_o + base * D + lane * CPL;  // split k at orow + k * D
+    const float l0 = lane < S ? a.ws_lse[base + lane] : -INFINITY;
+    float2 pre[PRE][CPL / 2];
+#pragma unroll
+    for (int k = 0; k < PRE; ++k)
+#pragma unroll
+        for (int c = 0; c < CPL / 2; ++c)
+            pre[k][c] = k < S ? *reinterpret_cast<const float2 *>(orow + k * D + 2 * c) : make_float2(0.f, 0.f);
+    float M = l0;
+    for (int s0 = 32; s0 < S; s0 += 32)
         if (s0 + lane < S) M = fmaxf(M, a.ws_lse[base + s0 + lane]);
 #pragma unroll
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    float tot = 0.f;
+    const float w0 = lane < S ? __expf(l0 - M) : 0.f;
+    float tot = w0;
+#pragma unroll
+    for (int k = 0; k < PRE; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w0, k);  // 0 for k >= S
+#pragma unroll
+        for (int c = 0; c < CPL / 2; ++c) {
+            acc[2 * c] += wk * pre[k][c].x;
+            acc[2 * c + 1] += wk * pre[k][c].y;
+        }
+    }
     for (int s0 = 0; s0 < S; s0 += 32) {
-        const float w = s0 + lane < S ? __expf(a.ws_lse[base + s0 + lane] - M) : 0.f;
-        tot += w;
+        float w = w0;
+        if (s0 > 0) {
+            w = s0 + lane < S ? __expf(a.ws_lse[base + s0 + lane] - M) : 0.f;
+            tot += w;
+        }
         const int ns = min(32, S - s0);
-        for (int k = 0; k < ns; ++k) {
+        for (int k = s0 > 0 ? 0 : PRE; k < ns; ++k) {
             const float wk = __shfl_sync(0xffffffffu, w, k);
-            const float *src = a.ws_o + (base + s0 + k) * D + lane * CPL;
+            const float *src = orow + (int64_t)(s0 + k) * D;
 #pragma unroll
             for (int c = 0; c < CPL; c += 2) {
                 const float2 v = *reinterpret_cast<const float2 *>(src + c);
