@@ -290,3 +290,13 @@ def test_large_batch_short_contexts(split_tokens):
                                       head_dim=64, page_size=1, batch=1040, ctx_lo=1, ctx_hi=60,
                                       value_std=0.5, seed=81)
     run_case(case, split_tokens=split_tokens, max_splits=16)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_max_batch(fused):
+    """The largest batch the call accepts (4,096 requests), short contexts:
+    the per-request schedule prefix fills 16 KB of shared memory."""
+    case = workloads.make_decode_case("max-batch", num_layers=1, num_q_heads=8, num_kv_heads=2,
+                                      head_dim=128, page_size=1, batch=4096, ctx_lo=1, ctx_hi=24,
+                                      value_std=0.5, seed=82)
+    run_case(case, fused=fused)

@@ -123,3 +123,52 @@ def test_full_radix_shared_extend():
             ref, _ = orc.decode(qs, host[0], host[1], pt, sl, case.sm_scale)
             gu.check_attn(o[[a0 + t for t in ts]], ref, f"extend batch {bi} request {r}")
     assert mk.minisgl_debug_timeout_count() == 0
+
+
+def test_extend_long_context_full_budget():
+    """One launch at the chunk budget: a request extending 2,000 tokens over
+    24,000 cached ones beside a 6,192-token prefill with nothing cached (8,192
+    new tokens in all, GQA 4).  Sampled rows are checked against the oracle as
+    decodes over positions 0 .. C + t."""
+    cached, ext = [24000, 0], [2000, 6192]
+    Hq, Hkv = 32, 8
+    g = torch.Generator().manual_seed(2024)
+    lens = [c + e for c, e in zip(cached, ext)]
+    R = sum(lens) + 64
+    perm = torch.randperm(R - 1, generator=g).to(torch.int32)
+    W = workloads.align_up(max(lens))
+    pt = torch.full((2, W), R - 1, dtype=torch.int32)
+    locs, off = [], 0
+    for r, n in enumerate(lens):
+        pt[r, :n] = perm[off:off + n]
+        locs.append(perm[off + cached[r]:off + n])
+        off += n
+    case = workloads.ExtendCase(name="long-extend", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+                                num_rows=R, prefix_rows=perm[:0], extend_lens=list(ext),
+                                sm_scale=1 / 128 ** 0.5, value_std=0.5, seed=2024)
+    b = workloads.ExtendBatch(req_ids=[0, 1], cached_lens=torch.tensor(cached, dtype=torch.int32),
+                              extend_lens=torch.tensor(ext, dtype=torch.int32),
+                              q_offsets=torch.tensor([0, ext[0], ext[0] + ext[1]], dtype=torch.int32),
+                              page_table=pt, out_loc=torch.cat(locs).to(torch.int32))
+    case.batches.append(b)
+    assert b.total_tokens == 8192
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    host = (gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0]))
+    k, v, q = per_batch[0]
+    pool = mk.KVPool(pool_t)
+    mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+    o = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                               b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all()
+    orc = oracle.get()
+    orc.store_kv(host[0], host[1], k.cpu(), v.cpu(), b.out_loc)
+    gen = torch.Generator().manual_seed(5)
+    for r in range(2):
+        C, E, a0 = cached[r], ext[r], int(b.q_offsets[r])
+        ts = sorted({0, 1, 127, 128, E - 1, E // 2} | set(torch.randint(0, E, (6,), generator=gen).tolist()))
+        qs = q[[a0 + t for t in ts]].cpu()
+        sl = torch.tensor([C + t + 1 for t in ts], dtype=torch.int32)
+        ref, _ = orc.decode(qs, host[0], host[1], pt[r:r + 1].repeat(len(ts), 1), sl, case.sm_scale)
+        gu.check_attn(o[[a0 + t for t in ts]], ref, f"long extend request {r}")
+    assert mk.minisgl_debug_timeout_count() == 0
