@@ -19,6 +19,8 @@
 //     with 16-byte cp.async into the 128-byte-swizzled layout the tensor core
 //     reads (K as a K-major B operand, V as an MN-major B operand), two
 //     stages deep; completion is tracked by mbarriers (cp.async.mbarrier.arrive).
+//     A lane copies 4 chunks of each of its rows, so the address work per
+//     copy is small: these warps share schedulers with softmax warps.
 //   * Warp 11 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
 //     (M = N = 128) into tensor memory; O_X += P_X V with P_X read from
 //     tensor memory.  The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
@@ -26,7 +28,8 @@
 //   * Softmax warpgroups 0 (warps 0-3, tile A) and 1 (warps 4-7, tile B):
 //     thread i owns TMEM lane (= MMA row) i of its tile.  It reads its S row
 //     (64-column loads: maximum of the raw scores, then exponentials with
-//     packed f32x2 arithmetic), applies the causal limit C + t on diagonal
+//     packed f32x2 arithmetic; in the common path the next columns' load is
+//     in flight while the current ones are exponentiated), applies the causal limit C + t on diagonal
 //     tiles only, keeps a running max m and sum l (base 2), and writes
 //     P = 2^(s - m) as bf16 back into the upper 64 columns of its S row, where
 //     the PV MMA reads it.  O_X is rescaled in tensor memory only
@@ -191,6 +194,48 @@ __device__ __forceinline__ void exp_half(const uint32_t (&h)[64], uint64_t scale
         pw[e] = pack_bf16x2(p0, p1);
     }
 }
+// 2^(s*scale - m) for 32 scores: 16 bf16 pairs into pw[base ..]
+__device__ __forceinline__ void exp_quarter(const uint32_t (&h)[32], uint64_t scale2, uint64_t negm2,
+                                            uint64_t &lt, uint32_t (&pw)[32], int base) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        float x0, x1;
+        f2split(ffma2(f2(__uint_as_float(h[2 * e]), __uint_as_float(h[2 * e + 1])), scale2, negm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        lt = fadd2(lt, f2(p0, p1));
+        pw[base + e] = pack_bf16x2(p0, p1);
+    }
+}
+// tcgen05.wait::ld that the compiler sees as producing r: no use of r can be
+// scheduled before the wait
+__device__ __forceinline__ void tmem_wait_ld_dep(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                   "+r"(r[31])
+                 :
+                 : "memory");
+}
+// tcgen05.mma with each shared-memory descriptor given as its two 32-bit words
+__device__ __forceinline__ void tc_mma_bf16_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %6, 0;\n mov.b64 da, {%1, %2};\n"
+        " mov.b64 db, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %5, 0;\n mov.b64 db, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st16_from(uint32_t dst, const uint32_t (&pw)[32], int base) {
     uint32_t q[16];
 #pragma unroll
@@ -353,10 +398,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     SchedSlot *sched = &g_sched[slot];
     if (warp >= PRODUCER_WARP0 && warp < PRODUCER_WARP0 + PRODUCER_WARPS) {
         // ---------------- producer: Q_A, Q_B per item, then K/V tiles ----------------
-        // Thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31 of each
-        // 128-row tile (16 threads cover one 256-byte row).  An item's Q goes
-        // out with its first K/V tile, once the MMA warp has released the Q
-        // buffers (the previous item's last S is done).
+        // Q tiles: thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31
+        // (16 threads cover one 256-byte row).  K/V tiles: lane (rl = lane / 4,
+        // qq = lane % 4) of producer warp pw copies chunks qq, qq+4, qq+8,
+        // qq+12 of tokens 16m + 8pw + rl (m = 0..7), so one page-table entry
+        // and one address serve 8 copies; each warp instruction still writes
+        // 8 rows x 64 bytes that fall on distinct banks (4 wavefronts for 512
+        // bytes).  An item's Q goes out with its first K/V tile, once the MMA
+        // warp has released the Q buffers (the previous item's last S is done).
         constexpr int RPT = ROWS * 16 / PRODUCER_THREADS;  // rows per thread: 32
         const int pt = threadIdx.x - PRODUCER_WARP0 * 32;
         const int cc = pt & 15, tb = pt >> 4;
@@ -377,15 +426,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (cur.r < 0) break;
             const int32_t *ptab = a.page_table + (int64_t)cur.r * a.pt_stride;
             const int n_vis = cur.n_vis(), nkv = cur.nkv();
-            // each of the 16 threads sharing tb fetches 2 of its 32 rows; the
-            // rest come by shuffle within the half warp
+            // lane L fetches the page-table entries of tokens (m = L/8, rl = L%8)
+            // and (m = 4 + L/8, rl = L%8); the copying lanes get them by shuffle
+            const int pw = pt >> 5, rl = lane >> 2, qq = lane & 3;
             auto fetch2 = [&](int j, int &ra, int &rb) {
-                const int p = j * ROWS + tb * RPT + 2 * cc;
+                const int p = j * ROWS + 16 * (lane >> 3) + 8 * pw + (lane & 7);
                 ra = p < n_vis ? __ldg(ptab + p) : -1;
-                rb = p + 1 < n_vis ? __ldg(ptab + p + 1) : -1;
+                rb = p + 64 < n_vis ? __ldg(ptab + p + 64) : -1;
                 ra = ra < 0 ? -1 : min(ra, a.num_rows - 1);
                 rb = rb < 0 ? -1 : min(rb, a.num_rows - 1);
             };
+            // 128-byte swizzle: chunk c of token row t sits at 16-byte slot
+            // (c mod 8) xor (t mod 8); for c = qq + 4i that is one of these two
+            const uint32_t xo0 = (uint32_t)((qq ^ rl) << 4), xo1 = (uint32_t)(((qq ^ rl) ^ 4) << 4);
             int ra, rb;
             fetch2(0, ra, rb);
             for (int j = 0; j < nkv; ++j) {
@@ -408,14 +461,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const uint32_t sK = sKV + st * 2 * TILE_BYTES, sV = sK + TILE_BYTES;
 #pragma unroll
-                for (int k = 0; k < RPT; ++k) {
-                    const int tok = tb * RPT + k;
-                    const int row = __shfl_sync(0xffffffffu, (k & 1) ? rb : ra, (lane & 16) + (k >> 1));
-                    const int64_t e = (int64_t)max(row, 0) * a.row_stride + (int64_t)cur.g * D + cc * 8;
+                for (int mm = 0; mm < 8; ++mm) {
+                    const int row = __shfl_sync(0xffffffffu, mm < 4 ? ra : rb, ((mm & 3) << 3) | rl);
+                    const int64_t e = (int64_t)max(row, 0) * a.row_stride + (int64_t)cur.g * D + qq * 8;
                     const int bytes = row >= 0 ? 16 : 0;
-                    const uint32_t o = sw128(tok, cc);
-                    cp_async_16(sK + o, Kl + e, bytes);
-                    cp_async_16(sV + o, Vl + e, bytes);
+                    const uint32_t ob = (uint32_t)((2 * mm + pw) * 1024 + rl * 128);
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const uint32_t o = ob + (uint32_t)((ci >> 1) * HALF) + ((ci & 1) ? xo1 : xo0);
+                        cp_async_16(sK + o, Kl + e + 32 * ci, bytes);
+                        cp_async_16(sV + o, Vl + e + 32 * ci, bytes);
+                    }
                 }
                 cp_async_mbar_arrive_noinc(kv_full(st));
                 // next tile's rows: the loads are in flight while this thread
@@ -431,9 +487,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // couple of MMAs ahead, so whatever this thread executes between two
         // MMA groups leaves the tensor core idle.  Hence: the shared-memory
         // descriptors are built once here, and the one for K-slice kk of a
-        // tile is its tile's descriptor plus a constant (the 14-bit address
-        // field holds addr >> 4, below 2^14 for any shared-memory address, so
-        // the sum never carries into the next field); and a wait first probes
+        // tile is its tile's descriptor plus a constant, added to the lower
+        // 32-bit word only (the 14-bit address field holds addr >> 4, below
+        // 2^14 for any shared-memory address, so the sum never carries into
+        // the next field, and the upper word is the same for every Q and K
+        // tile, and for every V tile); and a wait first probes
         // the barrier once, taking the bounded, abort-aware path only when
         // the phase is not complete yet.
         if (lane == 0) {
@@ -453,28 +511,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const Item cur = *ring(n);
                 if (cur.r < 0) break;
                 const int nkv_a = cur.nkv_a, nkv_b = cur.nkv_b, nkv = cur.nkv();
+                const uint32_t dhi = (uint32_t)(dq0 >> 32);  // same upper word for every Q/K descriptor
+                const uint32_t vhi = (uint32_t)(dv0 >> 32);
                 auto issue_s = [&](int x, int j) {  // S_X(j) = Q_X K(j)^T
-                    const uint64_t dk = ((kv_iter + j) & 1) ? dk1 : dk0;
-                    const uint64_t dq = x ? dq1 : dq0;
+                    const uint32_t dk = (uint32_t)(((kv_iter + j) & 1) ? dk1 : dk0);
+                    const uint32_t dq = (uint32_t)(x ? dq1 : dq0);
                     const uint32_t ds = tmem + col_s(x);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         // K-slice kk of a K-major 128-byte-swizzled tile: 64-column
                         // region kk / 4, 32-byte step kk % 4 within the row
-                        const uint64_t off = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
-                        tc_mma_bf16(ds, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+                        const uint32_t off = (uint32_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+                        tc_mma_bf16_w(ds, dq + off, dhi, dk + off, dhi, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(s_full(x));
                 };
                 auto issue_pv = [&](int x, int j, uint32_t cnt) {  // O_X += P_X(j) V(j)
                     mwait(p_full(x), (cnt + j) & 1);
                     tc_fence_after();
-                    const uint64_t dv = ((kv_iter + j) & 1) ? dv1 : dv0;
+                    const uint32_t dv = (uint32_t)(((kv_iter + j) & 1) ? dv1 : dv0);
                     const uint32_t dO = tmem + col_o(x), dP = tmem + col_s(x) + 64;
 #pragma unroll
                     for (int kk = 0; kk < ROWS / 16; ++kk)  // 16 tokens (2 KB of V) per MMA
-                        tc_mma_bf16_ts(dO, dP + kk * 8, dv + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_bf16_ts_w(dO, dP + kk * 8, dv + (uint32_t)(kk * (2048 >> 4)), vhi, idesc_pv,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(pv_done(x));
                 };
                 auto wait_kv = [&](int j) {
@@ -551,16 +611,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint32_t p0[32], p1[32];
                         uint64_t lt = f2(0.f, 0.f);
                         {
-                            uint32_t h[64];
+                            // the second half's loads are in flight while the
+                            // previous part's exponentials run
+                            uint32_t h[64], c2[32], c3[32];
                             tmem_ld64(scol, h);
                             tmem_wait_ld();
+                            tmem_ld32(scol + 64, c2);
                             exp_half(h, scale2, negm2, lt, p0);
-                        }
-                        {
-                            uint32_t h[64];
-                            tmem_ld64(scol + 64, h);
-                            tmem_wait_ld();
-                            exp_half(h, scale2, negm2, lt, p1);
+                            tmem_wait_ld_dep(c2);
+                            tmem_ld32(scol + 96, c3);
+                            exp_quarter(c2, scale2, negm2, lt, p1, 0);
+                            tmem_wait_ld_dep(c3);
+                            exp_quarter(c3, scale2, negm2, lt, p1, 16);
                         }
                         float ta, tb;
                         f2split(lt, ta, tb);
