@@ -483,9 +483,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         cp_async_wait<0>();
     } else if (warp == MMA_WARP) {
         // ---------------- MMA issuer ----------------
-        // One thread issues every MMA, and the tensor core accepts only a
-        // couple of MMAs ahead, so whatever this thread executes between two
-        // MMA groups leaves the tensor core idle.  Hence: the shared-memory
+        // One thread (lane 0) issues every MMA, and the tensor core accepts
+        // only a couple of MMAs ahead, so whatever this thread executes between
+        // two MMA groups leaves the tensor core idle.  Hence: the whole warp
+        // runs the bookkeeping in step, with the loop bounds and the TMEM base
+        // passed through warp reductions so that every lane provably holds the
+        // same value (the compiler can then keep the counters and descriptors
+        // in uniform registers, which the MMA instruction reads), and only the
+        // MMA and commit instructions sit under `leader`; the shared-memory
         // descriptors are built once here, and the one for K-slice kk of a
         // tile is its tile's descriptor plus a constant, added to the lower
         // 32-bit word only (the 14-bit address field holds addr >> 4, below
@@ -494,7 +499,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // tile, and for every V tile); and a wait first probes
         // the barrier once, taking the bounded, abort-aware path only when
         // the phase is not complete yet.
-        if (lane == 0) {
+        {
+            const bool leader = lane == 0;
+            // the TMEM base is the same in every lane; a warp reduction makes
+            // that visible to the compiler
+            const uint32_t tm = __reduce_max_sync(0xffffffffu, tmem);
             const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
             const uint64_t dq1 = smem_desc_sw128(sQ + TILE_BYTES, 16, 1024);
             const uint64_t dk0 = smem_desc_sw128(sKV, 16, 1024);
@@ -507,35 +516,41 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t kv_iter = 0, cnt_a = 0, cnt_b = 0;
             for (uint32_t n = 0;; ++n) {
                 wait(item_ready(n), (n / RING) & 1);
-                if (*((volatile int *)&s_abort)) break;
                 const Item cur = *ring(n);
-                if (cur.r < 0) break;
-                const int nkv_a = cur.nkv_a, nkv_b = cur.nkv_b, nkv = cur.nkv();
+                const unsigned stop = (*((volatile int *)&s_abort) || cur.r < 0) ? 1u : 0u;
+                if (__reduce_max_sync(0xffffffffu, stop)) break;
+                const int nkv_a = (int)__reduce_max_sync(0xffffffffu, (unsigned)cur.nkv_a);
+                const int nkv_b = (int)__reduce_max_sync(0xffffffffu, (unsigned)cur.nkv_b);
+                const int nkv = max(nkv_a, nkv_b);
                 const uint32_t dhi = (uint32_t)(dq0 >> 32);  // same upper word for every Q/K descriptor
                 const uint32_t vhi = (uint32_t)(dv0 >> 32);
                 auto issue_s = [&](int x, int j) {  // S_X(j) = Q_X K(j)^T
                     const uint32_t dk = (uint32_t)(((kv_iter + j) & 1) ? dk1 : dk0);
                     const uint32_t dq = (uint32_t)(x ? dq1 : dq0);
-                    const uint32_t ds = tmem + col_s(x);
+                    const uint32_t ds = tm + col_s(x);
+                    if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        // K-slice kk of a K-major 128-byte-swizzled tile: 64-column
-                        // region kk / 4, 32-byte step kk % 4 within the row
-                        const uint32_t off = (uint32_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
-                        tc_mma_bf16_w(ds, dq + off, dhi, dk + off, dhi, idesc_qk, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            // K-slice kk of a K-major 128-byte-swizzled tile: 64-column
+                            // region kk / 4, 32-byte step kk % 4 within the row
+                            const uint32_t off = (uint32_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+                            tc_mma_bf16_w(ds, dq + off, dhi, dk + off, dhi, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(s_full(x));
                     }
-                    tc_commit(s_full(x));
                 };
                 auto issue_pv = [&](int x, int j, uint32_t cnt) {  // O_X += P_X(j) V(j)
                     mwait(p_full(x), (cnt + j) & 1);
                     tc_fence_after();
                     const uint32_t dv = (uint32_t)(((kv_iter + j) & 1) ? dv1 : dv0);
-                    const uint32_t dO = tmem + col_o(x), dP = tmem + col_s(x) + 64;
+                    const uint32_t dO = tm + col_o(x), dP = tm + col_s(x) + 64;
+                    if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < ROWS / 16; ++kk)  // 16 tokens (2 KB of V) per MMA
-                        tc_mma_bf16_ts_w(dO, dP + kk * 8, dv + (uint32_t)(kk * (2048 >> 4)), vhi, idesc_pv,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(pv_done(x));
+                        for (int kk = 0; kk < ROWS / 16; ++kk)  // 16 tokens (2 KB of V) per MMA
+                            tc_mma_bf16_ts_w(dO, dP + kk * 8, dv + (uint32_t)(kk * (2048 >> 4)), vhi,
+                                             idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(pv_done(x));
+                    }
                 };
                 auto wait_kv = [&](int j) {
                     mwait(kv_full((kv_iter + j) & 1), ((kv_iter + j) >> 1) & 1);
@@ -548,7 +563,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 wait_kv(0);
                 issue_s(0, 0);
                 if (nkv_b > 0) issue_s(1, 0);
-                if (nkv == 1) tc_commit(q_empty);
+                if (nkv == 1 && leader) tc_commit(q_empty);
                 for (int j = 0; j < nkv; ++j) {
                     bool next_ready = false;
                     if (j < nkv_a) issue_pv(0, j, cnt_a);
@@ -558,12 +573,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         issue_s(0, j + 1);
                     }
                     if (j < nkv_b) issue_pv(1, j, cnt_b);
-                    tc_commit(kv_empty((kv_iter + j) & 1));  // every MMA reading this stage is issued
+                    // every MMA reading this stage is issued
+                    if (leader) tc_commit(kv_empty((kv_iter + j) & 1));
                     if (j + 1 < nkv_b) {
                         if (!next_ready) wait_kv(j + 1);
                         issue_s(1, j + 1);
                     }
-                    if (j + 2 == nkv) tc_commit(q_empty);
+                    if (j + 2 == nkv && leader) tc_commit(q_empty);
                 }
                 kv_iter += nkv;
                 cnt_a += nkv_a;
