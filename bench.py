@@ -45,13 +45,15 @@ L2_BYTES = 129 * 2 ** 20
 # --------------------------------------------------------------------------- #
 def decode_layer_bytes(case) -> int:
     """Bytes one decode-attention call must move at minimum: each context
-    token's K and V row for every KV head, its page-table entry, the queries,
-    the outputs and seq_lens (real requests; padding requests read one row)."""
+    token's K and V row for every KV head (the padding requests all read one
+    dummy row, counted once), every page-table entry read, the queries, the
+    outputs and seq_lens."""
     Hkv, d, Hq = case.num_kv_heads, case.head_dim, case.num_q_heads
     ctx = int(case.seq_lens[:case.num_real].sum())
+    entries = int(case.seq_lens.sum())
     dummy = int(case.batch - case.num_real) > 0
     kv_rows = ctx + (1 if dummy else 0)
-    return (kv_rows * 2 * Hkv * d * 2 + ctx * 4 + case.batch * Hq * d * 2 * 2 + case.batch * 4)
+    return (kv_rows * 2 * Hkv * d * 2 + entries * 4 + case.batch * Hq * d * 2 * 2 + case.batch * 4)
 
 
 def store_layer_bytes(case) -> int:
