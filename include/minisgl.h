@@ -294,6 +294,32 @@ int minisgl_decode_attn_noalloc(const minisgl_kv_pool *pool, int32_t layer, cons
                                 int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
                                 float sm_scale, void *out, int32_t split_tokens, void *stream);
 
+/*
+ * Index check: a debugging aid with no counterpart in the pages, for callers
+ * who want to know whether their index tensors address rows outside the pool
+ * (the calls above never check index values on the device; they clamp them,
+ * with unspecified results).  It reads exactly the entries a decode or
+ * extend call over the same tensors would read and counts, on the device:
+ *   counts[0]: page_table[r, j] outside [0, num_rows), r < batch,
+ *              j < min(max(lens[r], 0), pt_width);
+ *   counts[1]: out_loc[i] outside [0, num_rows), i < n_out;
+ *   counts[2]: lens[r] outside [0, pt_width].
+ * The page_table rows are [learn, paged KV pool: page_table alignment
+ * passage] raw physical rows padded to pt_width; entries past a request's
+ * length are not read.
+ *   page_table: device int32, row r at page_table + r*pt_row_stride.
+ *   lens: device int32 [batch], the page-table positions each request reads
+ *      (seq_lens for decode; cached_lens + extend_lens for extend).
+ *   out_loc: device int32 [n_out] (may be NULL when n_out == 0).
+ *   counts: device uint32 [3], overwritten (zeroed on `stream`, then
+ *      counted); read them after the stream, e.g. with a copy to the host.
+ * No kernel traps or synchronises with the host.  batch == 0 and n_out == 0
+ * just zero the counts.
+ */
+int minisgl_check_indices(const int32_t *page_table, int32_t batch, int64_t pt_row_stride,
+                          int32_t pt_width, const int32_t *lens, const int32_t *out_loc,
+                          int32_t n_out, int32_t num_rows, uint32_t *counts, void *stream);
+
 /* Message of the last error on the calling thread ("" if none). */
 const char *minisgl_last_error(void);
 

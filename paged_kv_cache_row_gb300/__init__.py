@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
     minisgl_decode_attn(pool, layer, q, page_table, seq_lens, sm_scale, ...)
     minisgl_extend_attn(pool, layer, q, page_table, cached_lens, extend_lens, q_offsets, sm_scale, ...)
     minisgl_rope_store_kv(pool, layer, q, k, v, positions, cos_sin_cache, out_loc)
+    minisgl_check_indices(page_table, lens, num_rows, out_loc)   (debugging aid)
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ __all__ = [
     "minisgl_decode_workspace_bytes", "minisgl_device_sm_count", "minisgl_debug_timeout_count",
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
     "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv", "minisgl_cascade_decode_attn",
-    "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
+    "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn", "minisgl_check_indices",
 ]
 
 EXPORTED_SYMBOLS = [
@@ -34,6 +35,7 @@ EXPORTED_SYMBOLS = [
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
     "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
     "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
+    "minisgl_check_indices",
 ]
 
 MINISGL_BF16 = 1
@@ -88,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_store_decode_attn.argtypes = [P, i32, vp, vp, i64, i64, vp, vp, i32, vp, i32, i64, i32,
                                               vp, f32, vp, vp, sz, i32, vp]
     lib.minisgl_store_decode_attn.restype = ctypes.c_int
+    lib.minisgl_check_indices.argtypes = [vp, i32, i64, i32, vp, vp, i32, i32, vp, vp]
+    lib.minisgl_check_indices.restype = ctypes.c_int
     lib.minisgl_last_error.argtypes = []
     lib.minisgl_last_error.restype = ctypes.c_char_p
     lib.minisgl_device_sm_count.argtypes = []
@@ -286,6 +290,38 @@ def minisgl_extend_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: t
 
 def minisgl_device_sm_count() -> int:
     return int(load_library().minisgl_device_sm_count())
+
+
+def minisgl_check_indices(page_table: torch.Tensor, lens: torch.Tensor, num_rows: int,
+                          out_loc: Optional[torch.Tensor] = None, counts: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """Count, on the device, the index values a decode or extend call over
+    these tensors would read that lie outside the pool: returns an int32 CUDA
+    tensor [page-table entries, out_loc entries, lengths outside
+    [0, page_table width]] (read it after the stream).  lens is seq_lens for
+    decode, cached_lens + extend_lens for extend."""
+    lib = load_library()
+    _need(page_table, "page_table", torch.int32)
+    _need(lens, "lens", torch.int32)
+    if page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if lens.numel() != page_table.shape[0] or not lens.is_contiguous():
+        raise MinisglError("lens must be a contiguous [B] tensor")
+    n_out = 0
+    if out_loc is not None:
+        _need(out_loc, "out_loc", torch.int32)
+        if not out_loc.is_contiguous():
+            raise MinisglError("out_loc must be contiguous")
+        n_out = out_loc.numel()
+    if counts is None:
+        counts = torch.empty(3, dtype=torch.int32, device=page_table.device)
+    _need(counts, "counts", torch.int32)
+    if counts.numel() < 3:
+        raise MinisglError("counts needs 3 elements")
+    _check(lib.minisgl_check_indices(_ptr(page_table), page_table.shape[0], page_table.stride(0),
+                                     page_table.shape[1], _ptr(lens), _ptr(out_loc), n_out,
+                                     num_rows, _ptr(counts), _stream(stream)), "check_indices")
+    return counts
 
 
 def minisgl_debug_timeout_count() -> int:

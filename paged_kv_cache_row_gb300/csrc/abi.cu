@@ -515,4 +515,32 @@ int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, i
                        "rope_store_kv");
 }
 
+int minisgl_check_indices(const int32_t *page_table, int32_t batch, int64_t pt_row_stride,
+                          int32_t pt_width, const int32_t *lens, const int32_t *out_loc,
+                          int32_t n_out, int32_t num_rows, uint32_t *counts, void *stream) {
+    g_err.clear();
+    NvtxRange nvtx_range("minisgl_check_indices");
+    if (!counts) return fail(MINISGL_ERR_ARG, "check_indices: NULL counts");
+    if (batch < 0 || n_out < 0 || pt_width < 0)
+        return fail(MINISGL_ERR_ARG, "check_indices: negative batch, n_out or pt_width");
+    if (num_rows < 1) return fail(MINISGL_ERR_ARG, "check_indices: num_rows must be positive");
+    if (batch > 0 && (!page_table || !lens))
+        return fail(MINISGL_ERR_ARG, "check_indices: NULL page_table or lens");
+    if (n_out > 0 && !out_loc) return fail(MINISGL_ERR_ARG, "check_indices: NULL out_loc");
+    if (batch > 0 && pt_row_stride < pt_width)
+        return fail(MINISGL_ERR_SHAPE, "check_indices: need pt_width <= pt_row_stride");
+    minisgl::CheckArgs a;
+    a.page_table = page_table;
+    a.pt_stride = pt_row_stride;
+    a.pt_width = pt_width;
+    a.batch = batch;
+    a.lens = lens;
+    a.out_loc = out_loc;
+    a.n_out = n_out;
+    a.num_rows = num_rows;
+    a.counts = counts;
+    return cuda_status(minisgl::launch_check_indices(a, static_cast<cudaStream_t>(stream)),
+                       "check_indices");
+}
+
 }  // extern "C"

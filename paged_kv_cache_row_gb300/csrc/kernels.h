@@ -121,6 +121,18 @@ struct RopeStoreArgs {
 };
 cudaError_t launch_rope_store_kv(const RopeStoreArgs &a, cudaStream_t s);
 
+// Count index values outside the pool (a debugging aid; see minisgl_check_indices).
+struct CheckArgs {
+    const int32_t *page_table;
+    int64_t pt_stride;
+    int32_t pt_width, batch;
+    const int32_t *lens;          // [batch] page-table positions each request reads
+    const int32_t *out_loc;       // [n_out] or nullptr
+    int32_t n_out, num_rows;
+    uint32_t *counts;             // [3], zeroed by the caller's stream before the launch
+};
+cudaError_t launch_check_indices(const CheckArgs &a, cudaStream_t s);
+
 int device_sm_count();
 
 // Sets the calling thread's minisgl_last_error() message and returns `code`.

@@ -38,6 +38,17 @@ def test_library_exports_every_declared_symbol(lib):
     assert sorted(p.EXPORTED_SYMBOLS) == declared_symbols()
 
 
+def test_check_indices_rejects_bad_arguments_on_host(lib):
+    fake = 1 << 40  # never dereferenced: validation fails before any device work
+    assert lib.minisgl_check_indices(fake, 4, 32, 32, fake, fake, 4, 100, None, None) == -1
+    assert b"counts" in lib.minisgl_last_error()
+    assert lib.minisgl_check_indices(fake, -1, 32, 32, fake, fake, 4, 100, fake, None) == -1
+    assert lib.minisgl_check_indices(fake, 4, 32, 32, fake, fake, 4, 0, fake, None) == -1
+    assert lib.minisgl_check_indices(None, 4, 32, 32, fake, fake, 4, 100, fake, None) == -1
+    assert lib.minisgl_check_indices(fake, 4, 32, 32, fake, None, 4, 100, fake, None) == -1
+    assert lib.minisgl_check_indices(fake, 4, 16, 32, fake, fake, 4, 100, fake, None) == -3
+
+
 def test_error_codes_on_host(lib):
     import paged_kv_cache_row_gb300 as p
     fake = 1 << 40  # never dereferenced: every call below fails validation first
