@@ -259,8 +259,8 @@ def test_page_table_example_golden():
 
 
 def test_store_kv_strided_and_pagefirst():
-    """store_kv and decode on a PageFirst pool (pages outermost, permuted view)
-    with k/v taken as strided slices of a fused qkv buffer."""
+    """store_kv on a PageFirst pool (pages outermost, permuted view) with k/v
+    taken as strided slices of a fused qkv buffer; other layers untouched."""
     L, R, Hkv, d, N, Hq = 3, 300, 2, 128, 9, 8
     g = torch.Generator().manual_seed(8)
     base = (torch.randn((2, R, L, Hkv, d), generator=g) * 0.5).to(torch.bfloat16).to(DEV)

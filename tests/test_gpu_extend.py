@@ -194,3 +194,59 @@ def test_extend_matches_decode_on_last_token():
     torch.cuda.synchronize()
     err = (o[last.to(DEV)].float() - od.float()).abs().max().item()
     assert err <= 2 * gu.MAX_ABS
+
+
+def _pagefirst(layer_pool, L, layer, seed):
+    """A PageFirst pool (2, R, L, H_kv, d) in memory, seen as the logical
+    (2, L, R, H_kv, d) view, whose `layer` holds the generator's values of a
+    one-layer pool; the other layers hold other values."""
+    _, _, R, Hkv, d = layer_pool.shape
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    base = torch.empty((2, R, L, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
+    view = base.permute(0, 2, 1, 3, 4)
+    view[:, layer] = layer_pool[:, 0]
+    return view
+
+
+def test_extend_and_decode_on_pagefirst_pool():
+    """Extend and decode read a PageFirst pool (row stride L*H_kv*d, layer
+    stride H_kv*d) through the same descriptor: results match the oracle on
+    the layer's rows, and store_kv lands in that layer only."""
+    L, layer = 3, 1
+    case = workloads.make_extend_case("pagefirst-ext", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                                      num_reqs=3, prefix_len=150, ext_lo=40, ext_hi=230,
+                                      budget=512, seed=31)
+    pool1, per_batch = workloads.make_extend_values(case, DEV)
+    pool_t = _pagefirst(pool1, L, layer, 32)
+    assert pool_t.stride(2) == L * 4 * 128 and pool_t.stride(1) == 4 * 128
+    hk, hv = gu.u16(pool1[0, 0]), gu.u16(pool1[1, 0])
+    others = [gu.u16(pool_t[0, l]) for l in range(L) if l != layer]
+    pool = mk.KVPool(pool_t)
+    orc = oracle.get()
+    for b, (k, v, q) in zip(case.batches, per_batch):
+        mk.minisgl_store_kv(pool, layer, k, v, b.out_loc.to(DEV))
+        o = mk.minisgl_extend_attn(pool, layer, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                                   b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+        torch.cuda.synchronize()
+        orc.store_kv(hk, hv, k.cpu(), v.cpu(), b.out_loc)
+        assert np.array_equal(gu.u16(pool_t[0, layer]), hk)
+        ref = orc.extend(q.cpu(), hk, hv, b.page_table, b.cached_lens, b.extend_lens, case.sm_scale)
+        gu.check_attn(o, ref, "pagefirst extend")
+    now = [gu.u16(pool_t[0, l]) for l in range(L) if l != layer]
+    assert all(a.tobytes() == b.tobytes() for a, b in zip(now, others)), "other layers changed"
+
+    dcase = workloads.make_decode_case("pagefirst-dec", num_layers=1, num_q_heads=16, num_kv_heads=4,
+                                       head_dim=128, page_size=1, batch=6, ctx_lo=20, ctx_hi=600,
+                                       value_std=0.5, seed=33)
+    dpool1, k_new, v_new, q = workloads.make_decode_values(dcase, DEV)
+    dpool_t = _pagefirst(dpool1, L, layer, 34)
+    dk, dv = gu.u16(dpool1[0, 0]), gu.u16(dpool1[1, 0])
+    dpool = mk.KVPool(dpool_t)
+    mk.minisgl_store_kv(dpool, layer, k_new[0], v_new[0], dcase.out_loc.to(DEV))
+    out = mk.minisgl_decode_attn(dpool, layer, q[0], dcase.page_table.to(DEV), dcase.seq_lens.to(DEV),
+                                 dcase.sm_scale)
+    torch.cuda.synchronize()
+    orc.store_kv(dk, dv, k_new[0].cpu(), v_new[0].cpu(), dcase.out_loc)
+    ref, _ = orc.decode(q[0].cpu(), dk, dv, dcase.page_table, dcase.seq_lens, dcase.sm_scale)
+    gu.check_attn(out, ref, "pagefirst decode")
+    assert mk.minisgl_debug_timeout_count() == 0
