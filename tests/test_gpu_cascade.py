@@ -27,15 +27,23 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def run_cascade(case, shared_len, seq_override=None):
+def run_cascade(case, shared_len, seq_override=None, pagefirst=False):
     pool_t, k_new, v_new, q = workloads.make_decode_values(case, DEV)
     hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+    layer = 0
+    if pagefirst:  # the same rows as layer 1 of a 2-layer PageFirst pool
+        _, _, R, Hkv, d = pool_t.shape
+        g = torch.Generator(device=DEV).manual_seed(case.seed + 1)
+        base = torch.empty((2, R, 2, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
+        view = base.permute(0, 2, 1, 3, 4)
+        view[:, 1] = pool_t[:, 0]
+        pool_t, layer = view, 1
     pool = mk.KVPool(pool_t)
     seq = case.seq_lens.clone() if seq_override is None else seq_override
     pt, sl, loc = case.page_table.to(DEV), seq.to(DEV), case.out_loc.to(DEV)
-    mk.minisgl_store_kv(pool, 0, k_new[0], v_new[0], loc)
-    out = mk.minisgl_cascade_decode_attn(pool, 0, q[0], pt, sl, shared_len, case.sm_scale)
-    plain = mk.minisgl_decode_attn(pool, 0, q[0], pt, sl, case.sm_scale)
+    mk.minisgl_store_kv(pool, layer, k_new[0], v_new[0], loc)
+    out = mk.minisgl_cascade_decode_attn(pool, layer, q[0], pt, sl, shared_len, case.sm_scale)
+    plain = mk.minisgl_decode_attn(pool, layer, q[0], pt, sl, case.sm_scale)
     torch.cuda.synchronize()
     orc = oracle.get()
     orc.store_kv(hk, hv, k_new[0].cpu(), v_new[0].cpu(), case.out_loc)
@@ -89,3 +97,11 @@ def test_cascade_decode_shared_len_shorter_than_sharing():
 
 def test_cascade_decode_full_workload():
     run_cascade(workloads.decode_shared_prefix_qwen3(), 4096)
+
+
+def test_cascade_decode_pagefirst_pool():
+    """Cascade decode on layer 1 of a PageFirst pool (row stride 2*H_kv*d)."""
+    case = workloads.make_shared_prefix_decode_case("cascade-pagefirst", num_q_heads=16, num_kv_heads=4,
+                                                    head_dim=128, batch=12, prefix_len=400,
+                                                    suffix_lo=0, suffix_hi=150, seed=71)
+    run_cascade(case, 400, pagefirst=True)

@@ -48,10 +48,15 @@ def check_rope(gpu: torch.Tensor, x_in: torch.Tensor, ref: np.ndarray, what: str
     assert not bad.any(), f"{what}: {int(bad.sum())} elements off, max err {err.max():.3g}"
 
 
-def run_rope(Hq, Hkv, d, positions, out_loc, R, seed, max_pos, dummy_from=None, layers=1, layer=0):
+def run_rope(Hq, Hkv, d, positions, out_loc, R, seed, max_pos, dummy_from=None, layers=1, layer=0,
+             pagefirst=False):
     g = torch.Generator(device=DEV).manual_seed(seed)
     N = out_loc.numel()
-    pool_t = torch.empty((2, layers, R, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
+    if pagefirst:  # rows outermost in memory, seen as the logical (2, L, R, H_kv, d) view
+        base = torch.empty((2, R, layers, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
+        pool_t = base.permute(0, 2, 1, 3, 4)
+    else:
+        pool_t = torch.empty((2, layers, R, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
     q = torch.empty((N, Hq, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
     k = torch.empty((N, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
     v = torch.empty((N, Hkv, d), dtype=torch.bfloat16, device=DEV).normal_(0, 0.5, generator=g)
@@ -166,3 +171,13 @@ def test_rope_then_decode_matches_oracle():
     orc.store_kv(hk, hv, rk, v0.cpu(), case.out_loc)
     ref, _ = orc.decode(rq, hk, hv, case.page_table, case.seq_lens, case.sm_scale)
     gu.check_attn(out, ref, "rope -> store -> decode")
+
+
+def test_rope_store_kv_pagefirst_pool():
+    """RoPE + store_kv into layer 2 of a PageFirst pool (row stride 3*H_kv*d):
+    the rotated k rows land in that layer only."""
+    g = torch.Generator().manual_seed(61)
+    N, R, max_pos = 90, 300, 4000
+    pos = torch.randint(0, max_pos, (N,), generator=g).to(torch.int32)
+    loc = torch.randperm(R, generator=g)[:N].to(torch.int32)
+    run_rope(16, 4, 128, pos, loc, R, 62, max_pos, layers=3, layer=2, pagefirst=True)
