@@ -38,8 +38,9 @@
  *   - Element type is bf16 for K, V, Q and the output (MINISGL_BF16); index
  *     tensors are int32.  Strides are in elements.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream).  No call synchronises with the host, so every call can be
- *     captured in a CUDA graph as long as its pointers stay fixed.
+ *     stream).  No call synchronises with the host.  minisgl_store_decode_attn
+ *     and minisgl_extend_attn (with minisgl_store_kv) are tested captured in
+ *     a CUDA graph and replayed, with their pointers fixed.
  *   - Return value: MINISGL_OK, or a negative MINISGL_ERR_* code with a
  *     message available from minisgl_last_error().  Argument checks happen on
  *     the host before any launch; a launch failure returns MINISGL_ERR_CUDA.
