@@ -1,15 +1,20 @@
 #!/usr/bin/env python3
 """Benchmark of the paged KV-pool attention hot path on GB300.
 
-A step is one decode step of the Qwen3-0.6B-shaped workload (28 layers,
-batch 64, H_q 16, H_kv 8, head_dim 128, page_size 1, contexts U[512,4096]):
-per layer, store_kv of the 64 new tokens and split-KV decode attention, in
-one minisgl_store_decode_attn call (partial kernel, which also stores the new
+A step is one decode step of the Llama-3-8B-shaped workload, the largest
+decode configuration (32 layers, 200 real requests padded with 56 CUDA-Graph
+padding requests to batch 256, H_q 32, H_kv 8, head_dim 128, page_size 1,
+contexts log-uniform in [1024, 8192], pool 1.2x the live tokens): per layer,
+store_kv of the 256 new tokens and split-KV decode attention, in one
+minisgl_store_decode_attn call (partial kernel, which also stores the new
 rows, + LSE merge kernel); the same step as two calls (minisgl_store_kv, then
-minisgl_decode_attn) is reported beside it.  The metric is paged decode-attention
-HBM GB/s (algorithmic bytes / time) with tokens/s beside it; the extend
-(chunked-prefill) kernel is measured on the radix-shared extend workload in
-TFLOP/s as a second object.
+minisgl_decode_attn) is reported beside it.  The metric is paged
+decode-attention HBM GB/s (algorithmic bytes / time) with the step's tokens/s
+(200 real tokens per step) beside it.  Secondary objects: the Qwen3-0.6B
+28-layer step, the long 64-row-page layer, tiny-decode latency, store_kv of an
+8192-token extend batch, extend (chunked prefill) TFLOP/s on the radix-shared
+workload, fused RoPE + store_kv, a mixed chunk + decode batch, shared-prefix
+(cascade) decode, and programmatic dependent launch on/off.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
 
@@ -304,6 +309,347 @@ def oracle_all_cores(case, pool_t, k_new, v_new, q, budget_s=10.0):
 # --------------------------------------------------------------------------- #
 # GPU arm
 # --------------------------------------------------------------------------- #
+def ev_time(fn, reps, stream, before=None):
+    """Mean duration in ms of `fn` over `reps` calls, each bracketed by CUDA
+    events on the launching stream; `before` (an L2 flush) runs outside the
+    events before every call."""
+    evs = []
+    for _ in range(reps):
+        if before is not None:
+            before()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def headline_case(layers: int):
+    """The Llama-3-8B decode workload with its pool at 1.2x the live tokens,
+    or 1.05x when the device has too little free memory for that (the pool of
+    32 layers at 1.2x is about 108 GB)."""
+    free, _ = torch.cuda.mem_get_info()
+    case = workloads.decode_llama3_8b(num_layers=layers)
+    if workloads.decode_pool_bytes(case) + (8 << 30) > free:
+        case = workloads.decode_llama3_8b(num_layers=layers, pool_factor=1.05)
+        case.pool_factor = 1.05
+    else:
+        case.pool_factor = 1.2
+    return case
+
+
+def decode_step_fn(mk, case, pool, k_new, v_new, q, pt, sl, loc, outs, ws, fused=True):
+    """One decode step over all layers: per layer store_kv of the step's new
+    rows and split-KV decode + LSE merge, fused into one call or as two."""
+    L = case.num_layers
+
+    def step():
+        for l in range(L):
+            if fused:
+                mk.minisgl_store_decode_attn(pool, l, k_new[l], v_new[l], loc, q[l], pt, sl,
+                                             case.sm_scale, out=outs[l], workspace=ws)
+            else:
+                mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
+                mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, out=outs[l], workspace=ws)
+    return step
+
+
+def time_steps(step, steps, warmup, stream, world):
+    """Device time per step over exactly `steps` steps after `warmup`, with a
+    barrier and a synchronize on both sides, max over ranks."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1) / steps, world)
+
+
+def secondary_decode_step(mk, args, dev, stream, peaks, case):
+    """A whole multi-layer decode step of another workload (fused calls)."""
+    pool_t, k_new, v_new, q = workloads.make_decode_values(case, dev)
+    pool = mk.KVPool(pool_t, case.page_size)
+    pt, sl, loc = case.page_table.to(dev), case.seq_lens.to(dev), case.out_loc.to(dev)
+    ws = mk.decode_workspace(case.batch, case.num_q_heads, pool)
+    outs = torch.empty((case.num_layers,) + tuple(q.shape[1:]), dtype=torch.bfloat16, device=dev)
+    step = decode_step_fn(mk, case, pool, k_new, v_new, q, pt, sl, loc, outs, ws)
+    ms = time_steps(step, max(5, args.steps // 4), args.warmup, stream, 1)
+    layer_b = decode_layer_bytes(case) + store_layer_bytes(case)
+    gbs = case.num_layers * layer_b / (ms * 1e-3) / 1e9
+    res = {"workload": case.name, "layers": case.num_layers, "batch": case.batch,
+           "real_requests": case.num_real, "H_q": case.num_q_heads, "H_kv": case.num_kv_heads,
+           "page_size": case.page_size, "context_tokens": int(case.seq_lens[:case.num_real].sum()),
+           "call": "minisgl_store_decode_attn per layer", "ms_per_step": round(ms, 4),
+           "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+           "tokens_per_s": round(case.num_real / (ms * 1e-3), 1),
+           "l2": "inputs larger than L2 (%.2f GB of K/V per layer)" % (layer_b / 1e9)}
+    del pool_t, k_new, v_new, q, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_tiny(mk, args, dev, stream):
+    """Tiny decode (batch 4, GQA 4, d 64): latency of one store + decode."""
+    tc = workloads.decode_tiny()
+    tpool_t, tk, tv, tq = workloads.make_decode_values(tc, dev)
+    tpool = mk.KVPool(tpool_t)
+    tpt, tsl, tloc = tc.page_table.to(dev), tc.seq_lens.to(dev), tc.out_loc.to(dev)
+    tws = mk.decode_workspace(tc.batch, tc.num_q_heads, tpool)
+    tout = torch.empty_like(tq[0])
+
+    def t_fused():
+        mk.minisgl_store_decode_attn(tpool, 0, tk[0], tv[0], tloc, tq[0], tpt, tsl, tc.sm_scale,
+                                     out=tout, workspace=tws)
+
+    def t_two():
+        mk.minisgl_store_kv(tpool, 0, tk[0], tv[0], tloc)
+        mk.minisgl_decode_attn(tpool, 0, tq[0], tpt, tsl, tc.sm_scale, out=tout, workspace=tws)
+
+    reps = max(50, args.steps)
+    for fn in (t_fused, t_two):
+        for _ in range(args.warmup):
+            fn()
+    return {"workload": tc.name, "batch": tc.batch, "context_tokens": int(tc.seq_lens.sum()),
+            "us_store_decode_fused": round(ev_time(t_fused, reps, stream) * 1e3, 2),
+            "us_store_kv_then_decode": round(ev_time(t_two, reps, stream) * 1e3, 2),
+            "reps": reps, "note": "latency bound: the whole pool (4 MB) stays in L2"}
+
+
+def bench_store_kv_at_scale(mk, args, dev, stream, peaks, flush):
+    """store_kv of the first radix-shared extend batch's 8192 new tokens
+    (67 MB moved), L2 flushed before every timed launch."""
+    ecase = workloads.extend_radix_shared()
+    epool_t, per_batch = workloads.make_extend_values(ecase, dev)
+    epool = mk.KVPool(epool_t)
+    k0, v0, _ = per_batch[0]
+    loc0 = ecase.batches[0].out_loc.to(dev)
+    n0 = int(loc0.numel())
+    s_b = n0 * (2 * 2 * ecase.num_kv_heads * ecase.head_dim * 2 + 4)
+    for _ in range(args.warmup):
+        mk.minisgl_store_kv(epool, 0, k0, v0, loc0)
+    s_ms = ev_time(lambda: mk.minisgl_store_kv(epool, 0, k0, v0, loc0), max(10, args.steps // 4),
+                   stream, before=flush)
+    res = {"workload": ecase.name + " batch 0", "tokens": n0, "algorithmic_bytes": s_b,
+           "ms_per_launch": round(s_ms, 5), "achieved_gbs": round(s_b / (s_ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm": round(s_b / (s_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+           "traffic": profile_traffic("store_kv.cu", "store_kv_extend_batch.md"),
+           "l2": "flushed (256 MB write) before every timed launch"}
+    del epool_t, per_batch
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_extend(mk, args, dev, stream, peaks, flush):
+    """store_kv + extend per chunked-prefill batch of the radix-shared
+    workload (TFLOP/s of causal-visible FLOPs), and fused RoPE + store_kv
+    over the same batches."""
+    ecase = workloads.extend_radix_shared()
+    epool_t, per_batch = workloads.make_extend_values(ecase, dev)
+    epool = mk.KVPool(epool_t)
+    eargs = [(b.page_table.to(dev), b.cached_lens.to(dev), b.extend_lens.to(dev),
+              b.q_offsets.to(dev), b.out_loc.to(dev)) for b in ecase.batches]
+    eouts = [torch.empty_like(qq) for _, _, qq in per_batch]
+
+    def estep():
+        for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
+            mk.minisgl_store_kv(epool, 0, k, v, eloc)
+            mk.minisgl_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, ecase.sm_scale, out=eo)
+
+    for _ in range(args.warmup):
+        estep()
+    torch.cuda.synchronize()
+    eks = max(5, args.steps // 10)
+    xev = []
+    for _ in range(eks):
+        for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
+            flush()  # q, out and the batch's rows (~170 MB) would partly stay in L2
+            mk.minisgl_store_kv(epool, 0, k, v, eloc)
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            mk.minisgl_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, ecase.sm_scale, out=eo)
+            b_.record(stream)
+            xev.append((a, b_))
+    torch.cuda.synchronize()
+    ext_ms_per_pass = sum(a.elapsed_time(b_) for a, b_ in xev) / eks
+    fl = extend_flops(ecase)
+    tf = fl / (ext_ms_per_pass * 1e-3) / 1e12
+    launch_fl = fl / len(ecase.batches)
+    launch_ms = ext_ms_per_pass / len(ecase.batches)
+    ext = {
+        "workload": ecase.name, "metric": "extend-attn TFLOP/s (causal-visible FLOPs)",
+        "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_pass": round(ext_ms_per_pass, 4),
+        "batches": len(ecase.batches), "tokens": int(sum(ecase.extend_lens)),
+        "tokens_per_s": round(sum(ecase.extend_lens) / (ext_ms_per_pass * 1e-3), 1),
+        "l2": "flushed (256 MB write) before each batch's store_kv + timed extend call",
+        "roofline": {"bound": "tensor", "achieved": round(launch_fl / (launch_ms * 1e-3) / 1e12, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(launch_fl / (launch_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                     "traffic": profile_traffic("extend.cu", "extend_radix_shared.md"),
+                     "peak_source": peaks["source"] + " bf16 dense burst"},
+    }
+    # fused RoPE + store_kv over the same batches (the step before attention)
+    max_pos = max(int((b.cached_lens + b.extend_lens).max()) for b in ecase.batches)
+    table = workloads.rope_cos_sin_cache(ecase.head_dim, max_pos).to(dev)
+    epos = [workloads.extend_positions(b).to(dev) for b in ecase.batches]
+    rq = [qq.clone() for _, _, qq in per_batch]
+
+    def rstep():
+        for (k, v, _), qq, pp, (_, _, _, _, eloc) in zip(per_batch, rq, epos, eargs):
+            mk.minisgl_rope_store_kv(epool, 0, qq, k, v, pp, table, eloc)
+
+    for _ in range(args.warmup):
+        rstep()
+    r_ms = ev_time(rstep, eks, stream)
+    r_bytes = rope_store_bytes(ecase)
+    rope = {"workload": ecase.name + " (all batches)", "ms_per_pass": round(r_ms, 4),
+            "tokens": int(sum(ecase.extend_lens)),
+            "achieved_gbs": round(r_bytes / (r_ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(r_bytes / (r_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "algorithmic_bytes_per_pass": r_bytes,
+            "l2": "inputs larger than L2 (%.0f MB per pass)" % (r_bytes / 1e6)}
+    del epool_t, per_batch, rq, eouts
+    torch.cuda.empty_cache()
+    return ext, rope
+
+
+def bench_mixed(mk, args, dev, stream, flush):
+    """A mixed batch (chunked prefill + 64 decode requests): one extend
+    launch over all requests against extend over the chunk requests followed
+    by store_decode_attn over the decode requests."""
+    mc = workloads.mixed_chunk_decode()
+    mb = mc.batches[0]
+    mpool_t, mper = workloads.make_extend_values(mc, dev)
+    mpool = mk.KVPool(mpool_t)
+    mk_, mv_, mq_ = mper[0]
+    nd = mc.num_decode
+    nb = len(mb.req_ids) - nd
+    Tc = int(mb.q_offsets[nb])
+    m_pt, m_cl, m_el, m_qo, m_loc = (mb.page_table.to(dev), mb.cached_lens.to(dev), mb.extend_lens.to(dev),
+                                     mb.q_offsets.to(dev), mb.out_loc.to(dev))
+    mout = torch.empty_like(mq_)
+    c_pt, c_cl, c_el, c_qo = m_pt[:nb], m_cl[:nb], m_el[:nb], m_qo[:nb + 1]
+    d_pt, d_sl, d_loc = m_pt[nb:], (m_cl[nb:] + 1).contiguous(), m_loc[Tc:]
+    dws = mk.decode_workspace(nd, mc.num_q_heads, mpool)
+
+    def mixed_one():
+        mk.minisgl_store_kv(mpool, 0, mk_, mv_, m_loc)
+        mk.minisgl_extend_attn(mpool, 0, mq_, m_pt, m_cl, m_el, m_qo, mc.sm_scale, out=mout)
+
+    def mixed_split():
+        mk.minisgl_store_kv(mpool, 0, mk_[:Tc], mv_[:Tc], m_loc[:Tc])
+        mk.minisgl_extend_attn(mpool, 0, mq_[:Tc], c_pt, c_cl, c_el, c_qo, mc.sm_scale, out=mout[:Tc])
+        mk.minisgl_store_decode_attn(mpool, 0, mk_[Tc:], mv_[Tc:], d_loc, mq_[Tc:], d_pt, d_sl,
+                                     mc.sm_scale, out=mout[Tc:], workspace=dws)
+
+    for fn in (mixed_one, mixed_split):
+        for _ in range(args.warmup):
+            fn()
+    reps = max(5, args.steps // 10)
+    m1 = ev_time(mixed_one, reps, stream, before=flush)
+    m2 = ev_time(mixed_split, reps, stream, before=flush)
+    res = {"workload": mc.name, "chunk_tokens": Tc, "decode_requests": nd,
+           "ms_one_extend_launch": round(m1, 4), "ms_extend_then_store_decode": round(m2, 4),
+           "faster": "one extend launch" if m1 < m2 else "extend + store_decode_attn",
+           "calls_one": "store_kv + extend_attn over all requests",
+           "calls_split": "store_kv + extend_attn over the chunk requests, then store_decode_attn "
+                          "over the decode requests",
+           "l2": "flushed (256 MB write) before every timed pass"}
+    del mpool_t, mper, mout
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_cascade(mk, args, dev, stream, peaks, flush):
+    """Shared-prefix (cascade) decode against plain decode on radix-shared
+    batches with a 4096- and a 1024-token prefix."""
+    casc = []
+    for sc in (workloads.decode_shared_prefix_qwen3(),
+               workloads.decode_shared_prefix_qwen3(prefix_len=1024)):
+        spool_t, sk, sv, sq = workloads.make_decode_values(sc, dev)
+        spool = mk.KVPool(spool_t)
+        spt, ssl, sloc = sc.page_table.to(dev), sc.seq_lens.to(dev), sc.out_loc.to(dev)
+        mk.minisgl_store_kv(spool, 0, sk[0], sv[0], sloc)
+        sout = torch.empty_like(sq[0])
+        runs = {
+            "cascade": lambda: mk.minisgl_cascade_decode_attn(spool, 0, sq[0], spt, ssl, sc.shared_len,
+                                                              sc.sm_scale, out=sout),
+            "plain": lambda: mk.minisgl_decode_attn(spool, 0, sq[0], spt, ssl, sc.sm_scale, out=sout),
+        }
+        t_ms = {}
+        for nm, fn in runs.items():
+            for _ in range(args.warmup):
+                fn()
+            t_ms[nm] = ev_time(fn, max(10, args.steps // 10), stream, before=flush)
+        plain_b = decode_layer_bytes(sc)
+        casc_b = cascade_layer_bytes(sc)
+        casc.append({"workload": sc.name, "shared_len": sc.shared_len,
+                     "ms_cascade": round(t_ms["cascade"], 5),
+                     "ms_plain_decode": round(t_ms["plain"], 5),
+                     "speedup": round(t_ms["plain"] / t_ms["cascade"], 3),
+                     "algorithmic_bytes_cascade": casc_b, "algorithmic_bytes_plain": plain_b,
+                     "achieved_gbs_cascade": round(casc_b / (t_ms["cascade"] * 1e-3) / 1e9, 1),
+                     "frac_of_hbm_cascade": round(casc_b / (t_ms["cascade"] * 1e-3) / 1e9
+                                                  / peaks["hbm_gbs"], 4),
+                     "l2": "flushed (256 MB write) before every timed call"})
+        del spool_t, sk, sv, sq
+        torch.cuda.empty_cache()
+    return casc
+
+
+PARTS = ("qwen3_step", "long_page64", "tiny", "store_kv", "extend", "mixed", "cascade")
+
+
+def secondary_objects(mk, args, dev, stream, peaks, st_ms=None, B=None, st_b=None, parts=PARTS):
+    extras = {}
+    flush_buf = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    flush = flush_buf.zero_
+    if "qwen3_step" in parts:
+        extras["qwen3_0p6b_step"] = secondary_decode_step(mk, args, dev, stream, peaks,
+                                                          workloads.decode_qwen3_0p6b())
+    if "long_page64" in parts:
+        extras["long_page64_layer"] = secondary_decode_step(mk, args, dev, stream, peaks,
+                                                            workloads.decode_long_page64())
+    if "tiny" in parts:
+        extras["tiny_decode_latency"] = bench_tiny(mk, args, dev, stream)
+    if "store_kv" in parts:
+        extras["store_kv"] = bench_store_kv_at_scale(mk, args, dev, stream, peaks, flush)
+        if st_ms is not None:
+            extras["store_kv"]["headline_layer_store"] = {
+                "tokens": B, "ms_per_launch": round(st_ms, 5),
+                "achieved_gbs": round(st_b / (st_ms * 1e-3) / 1e9, 1),
+                "note": "one row per request: launch-latency bound"}
+    if "extend" in parts:
+        extras["extend"], extras["rope_store_kv"] = bench_extend(mk, args, dev, stream, peaks, flush)
+    if "mixed" in parts:
+        extras["mixed_batch"] = bench_mixed(mk, args, dev, stream, flush)
+    if "cascade" in parts:
+        extras["cascade_decode"] = bench_cascade(mk, args, dev, stream, peaks, flush)
+    del flush_buf
+    torch.cuda.empty_cache()
+    return extras
+
+
+def run_part(args):
+    """One secondary object alone (for profiler captures on a small footprint)."""
+    import paged_kv_cache_row_gb300 as mk
+    from paged_kv_cache_row_gb300 import build as mkbuild
+    mkbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    out = secondary_objects(mk, args, dev, torch.cuda.current_stream(), measured_peaks(),
+                            parts=(args.part,))
+    print(json.dumps({"part": args.part, **out}), flush=True)
+
+
+
 def run_gpu(args, world, rank, local):
     import paged_kv_cache_row_gb300 as mk
     from paged_kv_cache_row_gb300 import build as mkbuild
@@ -312,21 +658,17 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = measured_peaks()
+    stream = torch.cuda.current_stream()
 
-    case = workloads.decode_qwen3_0p6b(num_layers=args.layers)
+    # ================= headline: Llama-3-8B decode step, 32 layers ================= #
+    case = headline_case(args.layers)
     L, B, Hq, Hkv, d = case.num_layers, case.batch, case.num_q_heads, case.num_kv_heads, case.head_dim
     pool_t, k_new, v_new, q = workloads.make_decode_values(case, dev)
     pool = mk.KVPool(pool_t, case.page_size)
     pt, sl, loc = case.page_table.to(dev), case.seq_lens.to(dev), case.out_loc.to(dev)
     ws = mk.decode_workspace(B, Hq, pool)
     outs = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(kk=k_new, vv=v_new, qq=q, ptab=pt, seq=sl, oloc=loc):
-        # per layer: store_kv of the 64 new rows fused into split-KV decode + LSE merge
-        for l in range(L):
-            mk.minisgl_store_decode_attn(pool, l, kk[l], vv[l], oloc, qq[l], ptab, seq, case.sm_scale,
-                                         out=outs[l], workspace=ws)
+    step = decode_step_fn(mk, case, pool, k_new, v_new, q, pt, sl, loc, outs, ws, fused=True)
 
     for _ in range(args.warmup):
         step()
@@ -347,8 +689,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
-    ms_local = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms_local, world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
     dec_b = decode_layer_bytes(case)
     st_b = store_layer_bytes(case)
@@ -357,25 +698,25 @@ def run_gpu(args, world, rank, local):
     tokens_s = job_rate(case.num_real, world, ms)
 
     # ---- the same step as two calls per layer: store_kv, then decode_attn ----
-    def fstep():
-        for l in range(L):
-            mk.minisgl_store_kv(pool, l, k_new[l], v_new[l], loc)
-            mk.minisgl_decode_attn(pool, l, q[l], pt, sl, case.sm_scale, out=outs[l], workspace=ws)
+    two_step = decode_step_fn(mk, case, pool, k_new, v_new, q, pt, sl, loc, outs, ws, fused=False)
+    fms = time_steps(two_step, args.steps, args.warmup, stream, world)
 
-    for _ in range(args.warmup):
-        fstep()
-    torch.cuda.synchronize()
-    barrier(world)
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for _ in range(args.steps):
-        fstep()
-    g1.record(stream)
-    torch.cuda.synchronize()
-    fms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world)
+    # ---- programmatic dependent launch off, then on again (same process, same order) ----
+    pdl_ab = None
+    if not args.no_extend:
+        ab_steps = max(5, args.steps // 2)
+        mk.minisgl_debug_set_pdl(False)
+        ms_off = time_steps(step, ab_steps, args.warmup, stream, world)
+        mk.minisgl_debug_set_pdl(True)
+        ms_on = time_steps(step, ab_steps, args.warmup, stream, world)
+        pdl_ab = {"workload": case.name, "steps": ab_steps,
+                  "ms_per_step_pdl_off": round(ms_off, 4), "ms_per_step_pdl_on": round(ms_on, 4),
+                  "ms_per_step_pdl_on_timed_region": round(ms, 4),
+                  "gain": round(ms_off / ms_on - 1.0, 4),
+                  "switch": "minisgl_debug_set_pdl (launch attribute on/off, same library)"}
 
     # ---- per-call durations of the dominant call, CUDA events on the launch stream ----
-    n_rep = max(3, min(args.steps, 50))
+    n_rep = max(3, min(args.steps, 20))
     ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(n_rep * L)]
     i = 0
     for _ in range(n_rep):
@@ -396,95 +737,7 @@ def run_gpu(args, world, rank, local):
     fused_ms = statistics.mean(c.elapsed_time(d_) for _, _, c, d_ in ev)
     achieved = (dec_b + st_b) / (fused_ms * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
-    traffic = profile_traffic("decode.cu", "decode_qwen3_0p6b.md")
-
-    # ---- the other decode workloads, one layer each: per-call GB/s and tokens/s ----
-    others = None
-    if not args.no_extend:
-        others = []
-        for oc in (workloads.decode_llama3_8b(num_layers=1), workloads.decode_long_page64()):
-            opool_t, ok_, ov_, oq = workloads.make_decode_values(oc, dev)
-            opool = mk.KVPool(opool_t, oc.page_size)
-            opt, osl, oloc = oc.page_table.to(dev), oc.seq_lens.to(dev), oc.out_loc.to(dev)
-            ows = mk.decode_workspace(oc.batch, oc.num_q_heads, opool)
-            oout = torch.empty_like(oq[0])
-
-            def ostep_fused():
-                mk.minisgl_store_decode_attn(opool, 0, ok_[0], ov_[0], oloc, oq[0], opt, osl, oc.sm_scale,
-                                             out=oout, workspace=ows)
-
-            def ostep_two():
-                mk.minisgl_store_kv(opool, 0, ok_[0], ov_[0], oloc)
-                mk.minisgl_decode_attn(opool, 0, oq[0], opt, osl, oc.sm_scale, out=oout, workspace=ows)
-
-            def otime(fn):
-                for _ in range(args.warmup):
-                    fn()
-                torch.cuda.synchronize()
-                oev = []
-                for _ in range(max(10, args.steps // 10)):
-                    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    fn()
-                    b_.record(stream)
-                    oev.append((a, b_))
-                torch.cuda.synchronize()
-                return statistics.mean(a.elapsed_time(b_) for a, b_ in oev)
-
-            oms = otime(ostep_fused)
-            oms_two = otime(ostep_two)
-            ob = decode_layer_bytes(oc) + store_layer_bytes(oc)
-            others.append({"workload": oc.name, "batch": oc.batch, "real_requests": oc.num_real,
-                           "H_q": oc.num_q_heads, "H_kv": oc.num_kv_heads, "page_size": oc.page_size,
-                           "context_tokens": int(oc.seq_lens[:oc.num_real].sum()),
-                           "call": "minisgl_store_decode_attn",
-                           "ms_per_layer": round(oms, 5),
-                           "two_call_ms_per_layer": round(oms_two, 5),
-                           "achieved_gbs": round(ob / (oms * 1e-3) / 1e9, 1),
-                           "frac_of_hbm": round(ob / (oms * 1e-3) / 1e9 / peak, 4),
-                           "tokens_per_s_per_layer": round(oc.num_real / (oms * 1e-3), 1),
-                           "l2": "inputs larger than L2 (%.1f GB of K/V per call)" % (ob / 1e9)})
-            del opool_t, ok_, ov_, oq
-
-    # ---- shared-prefix (cascade) decode vs plain decode on one radix-shared batch ----
-    casc = None
-    if not args.no_extend:
-        sc = workloads.decode_shared_prefix_qwen3()
-        spool_t, sk, sv, sq = workloads.make_decode_values(sc, dev)
-        spool = mk.KVPool(spool_t)
-        spt, ssl, sloc = sc.page_table.to(dev), sc.seq_lens.to(dev), sc.out_loc.to(dev)
-        mk.minisgl_store_kv(spool, 0, sk[0], sv[0], sloc)
-        sout = torch.empty_like(sq[0])
-        flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
-        runs = {
-            "cascade": lambda: mk.minisgl_cascade_decode_attn(spool, 0, sq[0], spt, ssl, sc.shared_len,
-                                                              sc.sm_scale, out=sout),
-            "plain": lambda: mk.minisgl_decode_attn(spool, 0, sq[0], spt, ssl, sc.sm_scale, out=sout),
-        }
-        t_ms = {}
-        for nm, fn in runs.items():
-            for _ in range(args.warmup):
-                fn()
-            torch.cuda.synchronize()
-            evs = []
-            for _ in range(max(10, args.steps // 10)):
-                flush.zero_()  # the 4096-row prefix (33 MB) would otherwise stay in L2
-                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn()
-                b_.record(stream)
-                evs.append((a, b_))
-            torch.cuda.synchronize()
-            t_ms[nm] = statistics.mean(a.elapsed_time(b_) for a, b_ in evs)
-        plain_b = decode_layer_bytes(sc)
-        casc_b = cascade_layer_bytes(sc)
-        casc = {"workload": sc.name, "ms_cascade": round(t_ms["cascade"], 5),
-                "ms_plain_decode": round(t_ms["plain"], 5),
-                "speedup": round(t_ms["plain"] / t_ms["cascade"], 3),
-                "algorithmic_bytes_cascade": casc_b, "algorithmic_bytes_plain": plain_b,
-                "achieved_gbs_cascade": round(casc_b / (t_ms["cascade"] * 1e-3) / 1e9, 1),
-                "l2": "flushed (256 MB write) before every timed call"}
-        del spool_t, sk, sv, sq, flush
+    traffic = profile_traffic("decode.cu", "decode_llama3_8b.md")
 
     # ---- e2e: the same step through the C ABI with host buffers ----
     pin = lambda t: t.cpu().pin_memory()
@@ -526,103 +779,13 @@ def run_gpu(args, world, rank, local):
                 h_out[l].copy_(outs[l], non_blocking=True)
         stream.wait_stream(d2h)
 
-    e2e_steps = max(3, args.steps // 4)
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    f1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world)
+    e2e_ms = time_steps(e2e_step, max(3, args.steps // 4), 2, stream, world)
     e2e_value = job_rate(step_bytes, world, e2e_ms) / 1e9
-
-    # ---- extend: radix-shared chunked prefill, store_kv + extend per batch ----
-    ext = None
-    rope = None
-    if not args.no_extend:
-        ecase = workloads.extend_radix_shared()
-        epool_t, per_batch = workloads.make_extend_values(ecase, dev)
-        epool = mk.KVPool(epool_t)
-        eargs = [(b.page_table.to(dev), b.cached_lens.to(dev), b.extend_lens.to(dev),
-                  b.q_offsets.to(dev), b.out_loc.to(dev)) for b in ecase.batches]
-        eouts = [torch.empty_like(qq) for _, _, qq in per_batch]
-
-        def estep():
-            for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
-                mk.minisgl_store_kv(epool, 0, k, v, eloc)
-                mk.minisgl_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, ecase.sm_scale, out=eo)
-
-        for _ in range(args.warmup):
-            estep()
-        torch.cuda.synchronize()
-        eks = max(5, args.steps // 10)
-        xev = []
-        eflush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
-        for _ in range(eks):
-            for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
-                eflush.zero_()  # q, out and the batch's rows (~170 MB) would partly stay in L2
-                mk.minisgl_store_kv(epool, 0, k, v, eloc)
-                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                mk.minisgl_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, ecase.sm_scale, out=eo)
-                b_.record(stream)
-                xev.append((a, b_))
-        torch.cuda.synchronize()
-        ext_ms_per_pass = sum(a.elapsed_time(b_) for a, b_ in xev) / eks
-        fl = extend_flops(ecase)
-        tf = fl / (ext_ms_per_pass * 1e-3) / 1e12
-        launch_fl = fl / len(ecase.batches)
-        launch_ms = ext_ms_per_pass / len(ecase.batches)
-        ext = {
-            "workload": ecase.name, "metric": "extend-attn TFLOP/s (causal-visible FLOPs)",
-            "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_pass": round(ext_ms_per_pass, 4),
-            "batches": len(ecase.batches), "tokens": int(sum(ecase.extend_lens)),
-            "l2": "flushed (256 MB write) before each batch's store_kv + timed extend call",
-            "roofline": {"bound": "tensor", "achieved": round(launch_fl / (launch_ms * 1e-3) / 1e12, 2),
-                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": round(launch_fl / (launch_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                         "traffic": profile_traffic("extend.cu", "extend_radix_shared.md"),
-                         "peak_source": peaks["source"] + " bf16 dense burst"},
-        }
-        # ---- fused RoPE + store_kv over the same batches (the step before attention) ----
-        max_pos = max(int((b.cached_lens + b.extend_lens).max()) for b in ecase.batches)
-        table = workloads.rope_cos_sin_cache(ecase.head_dim, max_pos).to(dev)
-        epos = [workloads.extend_positions(b).to(dev) for b in ecase.batches]
-        rq = [qq.clone() for _, _, qq in per_batch]
-
-        def rstep():
-            for (k, v, _), qq, pp, (_, _, _, _, eloc) in zip(per_batch, rq, epos, eargs):
-                mk.minisgl_rope_store_kv(epool, 0, qq, k, v, pp, table, eloc)
-
-        for _ in range(args.warmup):
-            rstep()
-        torch.cuda.synchronize()
-        rev = []
-        for _ in range(eks):
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            rstep()
-            b_.record(stream)
-            rev.append((a, b_))
-        torch.cuda.synchronize()
-        r_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in rev)
-        r_bytes = rope_store_bytes(ecase)
-        rope = {"workload": ecase.name + " (all batches)", "ms_per_pass": round(r_ms, 4),
-                "tokens": int(sum(ecase.extend_lens)),
-                "achieved_gbs": round(r_bytes / (r_ms * 1e-3) / 1e9, 1),
-                "frac_of_hbm": round(r_bytes / (r_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                "algorithmic_bytes_per_pass": r_bytes,
-                "l2": "inputs larger than L2 (%.0f MB per pass)" % (r_bytes / 1e6)}
-        del epool_t, per_batch, rq, eflush
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        reqs = list(range(0, B, 8))
+        reqs = list(range(0, case.num_real, 25))
         lay = sorted({0, L - 1})  # the first and the last layer
         run, nbytes = oracle_decode_sample(case, pool_t, k_new, v_new, q, lay, reqs)
         t0 = time.perf_counter()
@@ -635,52 +798,59 @@ def run_gpu(args, world, rank, local):
         dt = time.perf_counter() - t0
         cpu = {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
                "kind": "oracle",
-               "sample": f"store_kv + decode of requests {reqs} (of {B}) on layers {lay} "
-                         f"(every layer has the same lengths, so the rate holds for all {L}), "
+               "sample": f"store_kv + decode of requests {reqs} (of {case.num_real} real) on layers "
+                         f"{lay} (every layer has the same lengths, so the rate holds for all {L}), "
                          f"repeated {n}x, {dt:.1f} s, single-threaded fp64 C"}
         ac_v, ac_threads, ac_sample = oracle_all_cores(case, pool_t, k_new, v_new, q)
         cpu["all_cores"] = {"value": round(ac_v, 4), "unit": "GB/s", "cores": ac_threads,
                             "kind": "oracle", "sample": ac_sample}
 
+    head_cfg = {"workload": case.name, "layers": L, "batch": B, "real_requests": case.num_real,
+                "H_q": Hq, "H_kv": Hkv, "head_dim": d, "page_size": case.page_size,
+                "context_tokens": int(case.seq_lens[:case.num_real].sum()),
+                "pool_rows_per_layer": case.num_rows, "pool_factor": case.pool_factor,
+                "pool_gb": round(workloads.decode_pool_bytes(case) / 1e9, 1),
+                "l2": "inputs larger than L2: each layer reads %.2f GB of K/V, a step %.1f GB"
+                      % (dec_b / 1e9, step_bytes / 1e9),
+                "parallelism": f"dp{world} (independent batches per GPU)"}
+    del pool_t, k_new, v_new, q, outs, h_in, d_in, h_out, ws
+    torch.cuda.empty_cache()
+
+    # ================= secondary objects (not part of the headline) ================= #
+    extras = {} if args.no_extend else secondary_objects(mk, args, dev, stream, peaks, st_ms, B, st_b)
+
     gpu_launches = args.steps * L * 2  # per layer: decode partial (with the store) + LSE merge
     line = {
-        "metric": "paged decode-attn HBM GB/s (algorithmic bytes, store_kv + decode per layer)",
+        "metric": "paged decode-attn HBM GB/s (algorithmic bytes, store_kv + decode per layer) "
+                  "& tokens/s",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_s, 1),
-        "config": {"workload": case.name, "layers": L, "batch": B, "H_q": Hq, "H_kv": Hkv,
-                   "head_dim": d, "page_size": case.page_size,
-                   "context_tokens": int(case.seq_lens.sum()),
-                   "l2": "inputs larger than L2: each layer reads %.0f MB of K/V, a step %.1f GB"
-                         % (dec_b / 1e6, step_bytes / 1e9),
-                   "parallelism": f"dp{world} (independent batches per GPU)"},
+        "config": head_cfg,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "store_decode_attn call (split-KV partial kernel with the fused "
-                               "store, then the LSE merge kernel)",
+                               "store, then the LSE merge kernel), one layer",
                      "algorithmic_bytes_per_launch": dec_b + st_b, "ms_per_launch": round(fused_ms, 5),
                      "decode_attn_call_alone": {"ms": round(dec_ms, 5),
                                                 "achieved_gbs": round(dec_b / (dec_ms * 1e-3) / 1e9, 1)},
+                     "step_frac": round(value / world / peak, 4),
                      "peak_source": peaks["source"] + " hbm copy"},
         "two_call_step": {"ms_per_step": round(fms, 4),
-                                    "value": round(job_rate(step_bytes, world, fms) / 1e9, 2),
-                                    "unit": "GB/s",
-                                    "frac_of_hbm": round(job_rate(step_bytes, world, fms) / 1e9 / peak, 4)},
-        "store_kv": {"ms_per_launch": round(st_ms, 5),
-                     "achieved_gbs": round(st_b / (st_ms * 1e-3) / 1e9, 1)},
+                          "value": round(job_rate(step_bytes, world, fms) / 1e9, 2), "unit": "GB/s",
+                          "frac_of_hbm": round(job_rate(step_bytes, world, fms) / 1e9 / world / peak, 4)},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 4),
+                "tokens_per_s": round(job_rate(case.num_real, world, e2e_ms), 1),
                 "copies": "pinned host buffers; per-layer H2D and D2H on two copy streams, "
                           "overlapped with the layers, inside the timed region"},
         "gpu_launches": gpu_launches,
-        "extend": ext,
-        "rope_store_kv": rope,
-        "cascade_decode": casc,
-        "decode_other_workloads": others,
+        "pdl_ab": pdl_ab,
         "cpu_baseline": cpu,
     }
+    line.update(extras)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -691,10 +861,10 @@ def run_gpu(args, world, rank, local):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    case = workloads.decode_qwen3_0p6b()
+    case = workloads.decode_llama3_8b(num_layers=1)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     pool_t, k_new, v_new, q = workloads.make_decode_values(case, dev)
-    reqs = [0, 21, 42]
+    reqs = [0, 67, 134]
     run, nbytes = oracle_decode_sample(case, pool_t, k_new, v_new, q, [0], reqs)
     del pool_t
     for _ in range(args.warmup):
@@ -708,12 +878,14 @@ def run_reference(args, world, rank):
               f"layer 0 ({nbytes / 1e6:.1f} MB algorithmic), single-threaded fp64 C oracle")
     line = {
         "impl": "reference",
-        "metric": "paged decode-attn HBM GB/s (algorithmic bytes, store_kv + decode per layer)",
+        "metric": "paged decode-attn HBM GB/s (algorithmic bytes, store_kv + decode per layer) "
+                  "& tokens/s",
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": case.name, "layers": case.num_layers, "batch": case.batch,
-                   "sample_requests": reqs, "parallelism": "single CPU thread"},
+        "config": {"workload": case.name, "layers": 32, "batch": case.batch,
+                   "real_requests": case.num_real, "sample_requests": reqs,
+                   "parallelism": "single CPU thread"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores_used(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -728,11 +900,14 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
-    ap.add_argument("--layers", type=int, default=28,
-                    help="layers of the decode workload (28 = the full model; fewer only for "
-                         "profiler captures that must stay small)")
-    ap.add_argument("--no-extend", action="store_true")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="layers of the headline decode workload (32 = the full model; fewer only "
+                         "for profiler captures that must stay small)")
+    ap.add_argument("--no-extend", action="store_true",
+                    help="time the headline decode step only (no secondary workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", choices=PARTS, default=None,
+                    help="run one secondary object alone and print it (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -740,6 +915,9 @@ def main():
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, world, rank)
+        return
+    if args.part:
+        run_part(args)
         return
     world, rank, local = dist_setup(args.gpus)
     run_gpu(args, world, rank, local)

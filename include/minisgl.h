@@ -209,8 +209,11 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
 
 /*
  * Workspace size, in bytes, for minisgl_cascade_decode_attn with this batch
- * and head shape (room for up to 32 prefix chunks and 16 suffix splits); 0
- * for invalid sizes.
+ * and head shape; 0 for invalid sizes.  The number of prefix chunks a call
+ * may use (up to 32) grows with the SM count of the CURRENT device, so query
+ * the size with the device current that will run the call: a workspace sized
+ * on a device with fewer SMs can be too small for one with more (the call
+ * then fails with MINISGL_ERR_WORKSPACE).
  */
 size_t minisgl_cascade_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim);
@@ -281,11 +284,16 @@ int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, i
  * afford cudaMalloc/cudaFree synchronising the device.
  *   - Every GPU on which the library is loaded holds the 32 MiB array until the
  *     process exits.
- *   - The first call on each device (with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     with cudaGetSymbolAddress (a host-side lookup, never cached, so a
+ *     device reset cannot leave a stale address behind).  The first call on
+ *     each device also loads the library's module there: make that first
+ *     call before any stream capture.
  *   - Sizes whose scratch (minisgl_decode_workspace_bytes(..., 2)) exceeds
- *     32 MiB are rejected with MINISGL_ERR_WORKSPACE and a message.
+ *     32 MiB are rejected with MINISGL_ERR_WORKSPACE and a message: at
+ *     head_dim 128 that is about batch * num_q_heads > 32,500 (for example
+ *     16 query heads over 8 KV heads: batch 2028 fits, 2029 does not), at
+ *     head_dim 64 about batch * num_q_heads > 64,000.
  *   - All calls share the array: calls whose kernels can overlap on the GPU
  *     (unordered streams) race and give wrong results.  Nothing in the array
  *     needs to start at zero; every value a call reads, it wrote first.
@@ -327,6 +335,18 @@ const char *minisgl_last_error(void);
 /* Number of streaming multiprocessors of the current device (0 on error);
  * the persistent kernels size their grids from it. */
 int32_t minisgl_device_sm_count(void);
+
+/* Debugging and measurement aid: turn programmatic dependent launch on (1)
+ * or off (0) for every later launch of this library in the process, and
+ * return the previous setting.  With it on (the default, unless the
+ * environment held MINISGL_PDL=0 when the first launch was made) each kernel
+ * may be launched while the previous kernel in its stream is finishing and
+ * waits on the device for that kernel's results (griddepcontrol.wait); with
+ * it off every launch waits for the previous kernel to complete.  Results
+ * are the same either way; only the time between kernels changes.  Not
+ * thread-safe with respect to launches already being set up on other host
+ * threads. */
+int minisgl_debug_set_pdl(int enabled);
 
 /* Debugging aid: how many bounded waits inside the tensor-core kernels ran
  * out of time since the library was loaded on the current device.  A

@@ -28,6 +28,7 @@ __all__ = [
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
     "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv", "minisgl_cascade_decode_attn",
     "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn", "minisgl_check_indices",
+    "minisgl_debug_set_pdl",
 ]
 
 EXPORTED_SYMBOLS = [
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = [
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
     "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
     "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
-    "minisgl_check_indices",
+    "minisgl_check_indices", "minisgl_debug_set_pdl",
 ]
 
 MINISGL_BF16 = 1
@@ -98,6 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_device_sm_count.restype = i32
     lib.minisgl_debug_timeout_count.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.minisgl_debug_timeout_count.restype = ctypes.c_int
+    lib.minisgl_debug_set_pdl.argtypes = [ctypes.c_int]
+    lib.minisgl_debug_set_pdl.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -328,6 +331,12 @@ def minisgl_debug_timeout_count() -> int:
     c = ctypes.c_uint32(0)
     _check(load_library().minisgl_debug_timeout_count(ctypes.byref(c)), "debug_timeout_count")
     return int(c.value)
+
+
+def minisgl_debug_set_pdl(enabled: bool) -> bool:
+    """Turn programmatic dependent launch on or off for the library's later
+    launches (a measurement aid); returns the previous setting."""
+    return bool(load_library().minisgl_debug_set_pdl(1 if enabled else 0))
 
 
 def minisgl_rope_store_kv(pool: KVPool, layer: int, q: torch.Tensor, k: torch.Tensor,

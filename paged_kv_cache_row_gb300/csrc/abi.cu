@@ -4,6 +4,8 @@
 // carving, and the launches.  No entry point allocates device memory or
 // synchronises with the device.
 #include <algorithm>
+#include <atomic>
+#include <cstdlib>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -84,6 +86,20 @@ int check_heads(int32_t hq, int32_t hkv, int max_group, const char *who) {
 }  // namespace
 
 namespace minisgl {
+namespace {
+std::atomic<int> g_pdl{-1};  // -1: not read from the environment yet
+}
+bool pdl_enabled() {
+    int v = g_pdl.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char *e = std::getenv("MINISGL_PDL");
+        v = (e && e[0] == '0' && e[1] == '\0') ? 0 : 1;
+        int expect = -1;
+        if (!g_pdl.compare_exchange_strong(expect, v)) v = expect;
+    }
+    return v != 0;
+}
+
 int report_error(int code, const char *msg) {
     g_err = msg;
     return code;
@@ -107,6 +123,12 @@ extern "C" {
 const char *minisgl_last_error(void) { return g_err.c_str(); }
 
 int32_t minisgl_device_sm_count(void) { return minisgl::device_sm_count(); }
+
+int minisgl_debug_set_pdl(int enabled) {
+    const int prev = minisgl::pdl_enabled() ? 1 : 0;
+    minisgl::g_pdl.store(enabled ? 1 : 0);
+    return prev;
+}
 
 int minisgl_debug_timeout_count(uint32_t *count) {
     g_err.clear();

@@ -427,16 +427,18 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     if (wid >= a.batch * Hq) return;
     const int r = wid / Hq, h = wid - r * Hq, g = h / G;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (int64_t)wid * D + lane * CPL;
-    // two dependent rounds of loads: the context length and split count, then
-    // the first 32 LSEs together with the first PRE partial rows
+    // dependent rounds of loads: the context length, the split count (written
+    // by the partial kernel only for non-empty requests, so read after the
+    // empty check), then the first 32 LSEs together with the first PRE
+    // partial rows
     const int n = min(max(__ldg(a.seq_lens + r), 0), a.pt_width);
-    const int cnt = a.split_count[(int64_t)r * Hkv + g];
     if (n == 0) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) out[c] = __float2bfloat16_rn(0.f);
         if (a.lse_out && lane == 0) a.lse_out[wid] = -INFINITY;
         return;
     }
+    const int cnt = a.split_count[(int64_t)r * Hkv + g];
     const int S = min(cnt, a.max_splits);
     if (S <= 1) return;
     const int64_t base = (int64_t)wid * a.max_splits;

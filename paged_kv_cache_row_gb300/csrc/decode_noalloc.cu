@@ -14,9 +14,13 @@
 // The array (kNoallocScratchBytes = 32 MiB) is a file-scope static __device__
 // variable: every GPU on which the library is loaded holds one copy of it
 // until the process exits.  Host code cannot use the array's name as a device
-// address -- on the host it names a stand-in object -- so the first call on
-// each device, with that device current, looks the address up with
-// cudaGetSymbolAddress and caches it.  No call allocates or frees anything.
+// address -- on the host it names a stand-in object -- so every call, with
+// its device current, looks the address up with cudaGetSymbolAddress (a
+// host-side lookup) and checks the result.  Nothing is cached: if the caller
+// resets the device and the module is loaded again, the array may sit at a
+// new address, and a cached one would point at freed memory.  The first call
+// on a device also loads the library's module there, so make that first call
+// before any stream capture.  No call allocates or frees anything.
 //
 // Every call shares the one array and it keeps whatever the previous call
 // left in it.  Nothing in it has to start at zero: the partial kernel writes
@@ -25,7 +29,6 @@
 // on two streams without ordering between them) race on the array and give
 // wrong results; callers must order such calls.
 #include <cstdio>
-#include <mutex>
 
 #include "kernels.h"
 #include "minisgl.h"
@@ -36,24 +39,13 @@ constexpr size_t kNoallocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device, looked up on
+// every call (see above for why it is not cached).
 cudaError_t scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

@@ -7,6 +7,13 @@
 
 namespace minisgl {
 
+// Whether launches carry the programmatic-stream-serialization attribute
+// (on unless the environment holds MINISGL_PDL=0 when the library loads, or
+// minisgl_debug_set_pdl turned it off).  Kernels call griddepcontrol.wait
+// either way; without the attribute it returns at once because the launch
+// already waited for the previous kernel.
+bool pdl_enabled();
+
 // Launch with programmatic stream serialization, so this kernel's launch and
 // prologue overlap the tail of the previous kernel in the stream; the kernel
 // itself calls griddepcontrol.wait before touching global memory.
@@ -22,7 +29,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -157,20 +157,30 @@ def decode_tiny(seed: int = 1000) -> DecodeCase:
                             seed=seed)
 
 
-def decode_qwen3_0p6b(seed: int = 1001, num_layers: int = 28) -> DecodeCase:
+def decode_qwen3_0p6b(seed: int = 1001, num_layers: int = 28,
+                      pool_factor: float = 1.2) -> DecodeCase:
     """Qwen3-0.6B attention shapes: 28 layers, H_q 16, H_kv 8, d 128, batch 64, ctx U[512,4096]."""
     return make_decode_case("qwen3-0.6b-decode-b64-ctx512-4096", num_layers=num_layers,
                             num_q_heads=16, num_kv_heads=8, head_dim=128, page_size=1,
-                            batch=64, ctx_lo=512, ctx_hi=4096, value_std=0.5, seed=seed)
+                            batch=64, ctx_lo=512, ctx_hi=4096, value_std=0.5,
+                            pool_factor=pool_factor, seed=seed)
 
 
-def decode_llama3_8b(seed: int = 1002, num_layers: int = 32) -> DecodeCase:
+def decode_llama3_8b(seed: int = 1002, num_layers: int = 32,
+                     pool_factor: float = 1.2) -> DecodeCase:
     """Llama-3-8B attention shapes: 32 layers, H_q 32, H_kv 8, d 128; 200 real requests
-    with log-uniform ctx in [1024,8192], padded with 56 dummy requests to batch 256."""
+    with log-uniform ctx in [1024,8192], padded with 56 dummy requests to batch 256.
+    The pool holds pool_factor times the live tokens (1.2; 1.05 where memory is short)."""
     return make_decode_case("llama3-8b-decode-b200pad256-ctx1k-8k", num_layers=num_layers,
                             num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=1,
                             batch=256, num_dummy=56, ctx_lo=1024, ctx_hi=8192,
-                            ctx_dist="loguniform", value_std=0.5, seed=seed)
+                            ctx_dist="loguniform", value_std=0.5, pool_factor=pool_factor,
+                            seed=seed)
+
+
+def decode_pool_bytes(case: DecodeCase) -> int:
+    """Bytes of the (2, L, R, H_kv, d) bf16 pool of a decode case."""
+    return 2 * case.num_layers * case.num_rows * case.num_kv_heads * case.head_dim * 2
 
 
 def decode_long_page64(seed: int = 1004) -> DecodeCase:
@@ -429,9 +439,60 @@ def make_shared_prefix_decode_case(name: str, *, num_q_heads: int, num_kv_heads:
     return case
 
 
-def decode_shared_prefix_qwen3(seed: int = 1005) -> DecodeCase:
+def decode_shared_prefix_qwen3(seed: int = 1005, prefix_len: int = 4096) -> DecodeCase:
     """Qwen3-0.6B-shaped decode (H_q 16, H_kv 8, d 128) for 64 requests that
-    share a 4096-token cached prefix and add private suffixes of U[16, 512]."""
-    return make_shared_prefix_decode_case("shared-prefix-decode-b64-p4096-s16-512", num_q_heads=16,
-                                          num_kv_heads=8, head_dim=128, batch=64, prefix_len=4096,
-                                          suffix_lo=16, suffix_hi=512, seed=seed)
+    share a cached prefix (4096 tokens by default) and add private suffixes
+    of U[16, 512]."""
+    return make_shared_prefix_decode_case(f"shared-prefix-decode-b64-p{prefix_len}-s16-512",
+                                          num_q_heads=16, num_kv_heads=8, head_dim=128, batch=64,
+                                          prefix_len=prefix_len, suffix_lo=16, suffix_hi=512,
+                                          seed=seed)
+
+
+# --------------------------------------------------------------------------- #
+# a mixed batch: chunked prefill and decode requests in one extend call
+# --------------------------------------------------------------------------- #
+def mixed_chunk_decode(seed: int = 1006, num_decode: int = 64, ctx_lo: int = 512,
+                       ctx_hi: int = 4096) -> ExtendCase:
+    """One mixed batch as SGLang's mixed-chunk mode forms it ("SGLang 源码导读",
+    --enable-mixed-chunk): the first chunked-prefill batch of the radix-shared
+    extend workload (requests sharing a 2048-token prefix, up to 8192 new
+    tokens) followed by `num_decode` decode requests, each adding one token
+    over U[ctx_lo, ctx_hi] cached tokens (the Qwen3-0.6B decode context mix);
+    H_q 32, H_kv 8, d 128.  Returns a one-batch ExtendCase; the decode
+    requests are the last `num_decode` of the batch (case.num_decode)."""
+    base = extend_radix_shared()
+    b0 = base.batches[0]
+    g = torch.Generator().manual_seed(seed)
+    ctx = torch.randint(ctx_lo, ctx_hi + 1, (num_decode,), generator=g).tolist()
+    live_base = base.num_rows - 2
+    n_dec_rows = sum(c + 1 for c in ctx)
+    R = live_base + n_dec_rows + 2
+    poison = R - 1
+    perm = (torch.randperm(n_dec_rows, generator=g) + live_base).to(torch.int32)
+    lens = [int(c) + int(e) for c, e in zip(b0.cached_lens.tolist(), b0.extend_lens.tolist())]
+    width = align_up(max(lens + [c + 1 for c in ctx]))
+    nb = len(lens)
+    pt = torch.full((nb + num_decode, width), poison, dtype=torch.int32)
+    for r, n in enumerate(lens):
+        pt[r, :n] = b0.page_table[r, :n]
+    outs = [b0.out_loc]
+    off = 0
+    for i, c in enumerate(ctx):
+        rows = perm[off:off + c + 1]
+        off += c + 1
+        pt[nb + i, :c + 1] = rows
+        outs.append(rows[c:c + 1])
+    cl = torch.cat([b0.cached_lens, torch.tensor(ctx, dtype=torch.int32)])
+    el = torch.cat([b0.extend_lens, torch.ones(num_decode, dtype=torch.int32)])
+    qo = torch.zeros(nb + num_decode + 1, dtype=torch.int32)
+    qo[1:] = torch.cumsum(el, 0)
+    case = ExtendCase(name=f"mixed-chunk8192-plus-{num_decode}-decode", num_q_heads=base.num_q_heads,
+                      num_kv_heads=base.num_kv_heads, head_dim=base.head_dim, num_rows=R,
+                      prefix_rows=base.prefix_rows, extend_lens=el.tolist(), sm_scale=base.sm_scale,
+                      value_std=base.value_std, seed=seed)
+    case.batches.append(ExtendBatch(req_ids=list(range(nb + num_decode)), cached_lens=cl.to(torch.int32),
+                                    extend_lens=el.to(torch.int32), q_offsets=qo.to(torch.int32),
+                                    page_table=pt, out_loc=torch.cat(outs).to(torch.int32)))
+    case.num_decode = num_decode  # type: ignore[attr-defined]
+    return case
