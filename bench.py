@@ -382,6 +382,10 @@ def secondary_decode_step(mk, args, dev, stream, peaks, case):
     outs = torch.empty((case.num_layers,) + tuple(q.shape[1:]), dtype=torch.bfloat16, device=dev)
     step = decode_step_fn(mk, case, pool, k_new, v_new, q, pt, sl, loc, outs, ws)
     ms = time_steps(step, max(5, args.steps // 4), args.warmup, stream, 1)
+    mk.minisgl_debug_set_pdl(False)
+    ms_off = time_steps(step, max(5, args.steps // 4), args.warmup, stream, 1)
+    mk.minisgl_debug_set_pdl(True)
+    ms_on = time_steps(step, max(5, args.steps // 4), args.warmup, stream, 1)
     layer_b = decode_layer_bytes(case) + store_layer_bytes(case)
     gbs = case.num_layers * layer_b / (ms * 1e-3) / 1e9
     res = {"workload": case.name, "layers": case.num_layers, "batch": case.batch,
@@ -390,6 +394,8 @@ def secondary_decode_step(mk, args, dev, stream, peaks, case):
            "call": "minisgl_store_decode_attn per layer", "ms_per_step": round(ms, 4),
            "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
            "tokens_per_s": round(case.num_real / (ms * 1e-3), 1),
+           "pdl_ab": {"ms_per_step_pdl_off": round(ms_off, 4), "ms_per_step_pdl_on": round(ms_on, 4),
+                      "gain": round(ms_off / ms_on - 1.0, 4)},
            "l2": "inputs larger than L2 (%.2f GB of K/V per layer)" % (layer_b / 1e9)}
     del pool_t, k_new, v_new, q, outs
     torch.cuda.empty_cache()
@@ -417,32 +423,66 @@ def bench_tiny(mk, args, dev, stream):
     for fn in (t_fused, t_two):
         for _ in range(args.warmup):
             fn()
+    torch.cuda.synchronize()
+
+    def graph_us(fn, n=20):
+        """Device time per call: n calls captured in one CUDA graph, replayed."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for _ in range(n):
+                fn()
+        for _ in range(3):
+            gr.replay()
+        return ev_time(gr.replay, 20, stream) * 1e3 / n
+
     return {"workload": tc.name, "batch": tc.batch, "context_tokens": int(tc.seq_lens.sum()),
-            "us_store_decode_fused": round(ev_time(t_fused, reps, stream) * 1e3, 2),
-            "us_store_kv_then_decode": round(ev_time(t_two, reps, stream) * 1e3, 2),
-            "reps": reps, "note": "latency bound: the whole pool (4 MB) stays in L2"}
+            "us_store_decode_fused": round(graph_us(t_fused), 2),
+            "us_store_kv_then_decode": round(graph_us(t_two), 2),
+            "timing": "device time per call: 20 calls captured in a CUDA graph, replayed 20x",
+            "us_per_python_call_fused": round(ev_time(t_fused, reps, stream) * 1e3, 2),
+            "us_per_python_call_two": round(ev_time(t_two, reps, stream) * 1e3, 2),
+            "python_call_note": "one call at a time through the Python binding: host-bound",
+            "note": "latency bound: the whole pool (4 MB) stays in L2"}
 
 
-def bench_store_kv_at_scale(mk, args, dev, stream, peaks, flush):
-    """store_kv of the first radix-shared extend batch's 8192 new tokens
-    (67 MB moved), L2 flushed before every timed launch."""
-    ecase = workloads.extend_radix_shared()
-    epool_t, per_batch = workloads.make_extend_values(ecase, dev)
-    epool = mk.KVPool(epool_t)
-    k0, v0, _ = per_batch[0]
-    loc0 = ecase.batches[0].out_loc.to(dev)
-    n0 = int(loc0.numel())
-    s_b = n0 * (2 * 2 * ecase.num_kv_heads * ecase.head_dim * 2 + 4)
+def bench_store_kv_at_scale(mk, args, dev, stream, peaks):
+    """store_kv of 8192-token batches (the chunked-prefill budget; 67 MB moved
+    per launch) in steady state: eight batches with disjoint rows and their
+    own k/v are stored one after the other, so each launch reads and writes
+    memory the previous seven have pushed out of the L2 (536 MB in all)."""
+    rot = workloads.store_rotation()
+    Hkv, d = rot.num_kv_heads, rot.head_dim
+    pool_t = workloads.make_pool(1, rot.num_rows, Hkv, d, 0.5, rot.seed, dev)
+    pool = mk.KVPool(pool_t)
+    g = torch.Generator(device=dev).manual_seed(rot.seed * 104729 + 7)
+    n = int(rot.out_locs[0].numel())
+    ks = [torch.empty((n, Hkv, d), dtype=torch.bfloat16, device=dev).normal_(0, 0.5, generator=g)
+          for _ in rot.out_locs]
+    vs = [torch.empty((n, Hkv, d), dtype=torch.bfloat16, device=dev).normal_(0, 0.5, generator=g)
+          for _ in rot.out_locs]
+    locs = [l.to(dev) for l in rot.out_locs]
+
+    def rotation():
+        for k, v, l in zip(ks, vs, locs):
+            mk.minisgl_store_kv(pool, 0, k, v, l)
+
     for _ in range(args.warmup):
-        mk.minisgl_store_kv(epool, 0, k0, v0, loc0)
-    s_ms = ev_time(lambda: mk.minisgl_store_kv(epool, 0, k0, v0, loc0), max(10, args.steps // 4),
-                   stream, before=flush)
-    res = {"workload": ecase.name + " batch 0", "tokens": n0, "algorithmic_bytes": s_b,
-           "ms_per_launch": round(s_ms, 5), "achieved_gbs": round(s_b / (s_ms * 1e-3) / 1e9, 1),
-           "frac_of_hbm": round(s_b / (s_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        rotation()
+    reps = max(5, args.steps // 4)
+    ms = ev_time(lambda: [rotation() for _ in range(reps)], 1, stream) / (reps * len(locs))
+    s_b = n * (2 * 2 * Hkv * d * 2 + 4)
+    res = {"workload": rot.name, "tokens": n, "algorithmic_bytes": s_b,
+           "ms_per_launch": round(ms, 5), "achieved_gbs": round(s_b / (ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm": round(s_b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "traffic": profile_traffic("store_kv.cu", "store_kv_extend_batch.md"),
-           "l2": "flushed (256 MB write) before every timed launch"}
-    del epool_t, per_batch
+           "launches_timed": reps * len(locs),
+           "l2": "8 batches with disjoint rows stored in turn: 536 MB per rotation, larger than L2"}
+    del pool_t, ks, vs
     torch.cuda.empty_cache()
     return res
 
@@ -495,6 +535,42 @@ def bench_extend(mk, args, dev, stream, peaks, flush):
                      "traffic": profile_traffic("extend.cu", "extend_radix_shared.md"),
                      "peak_source": peaks["source"] + " bf16 dense burst"},
     }
+    # the same batches through the shared-prefix (cascade) extend call
+    P = int(ecase.prefix_rows.numel())
+    Tmax = max(b.total_tokens for b in ecase.batches)
+    cws = torch.zeros(mk.minisgl_cascade_extend_workspace_bytes(Tmax, ecase.num_q_heads, ecase.head_dim),
+                      dtype=torch.uint8, device=dev)
+
+    def cstep():
+        for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
+            mk.minisgl_store_kv(epool, 0, k, v, eloc)
+            mk.minisgl_cascade_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, P, ecase.sm_scale, out=eo,
+                                           workspace=cws)
+
+    for _ in range(args.warmup):
+        cstep()
+    torch.cuda.synchronize()
+    cev = []
+    for _ in range(eks):
+        for (k, v, qq), (ept, ecl, eel, eqo, eloc), eo in zip(per_batch, eargs, eouts):
+            flush()
+            mk.minisgl_store_kv(epool, 0, k, v, eloc)
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            mk.minisgl_cascade_extend_attn(epool, 0, qq, ept, ecl, eel, eqo, P, ecase.sm_scale, out=eo,
+                                           workspace=cws)
+            b_.record(stream)
+            cev.append((a, b_))
+    torch.cuda.synchronize()
+    c_ms = sum(a.elapsed_time(b_) for a, b_ in cev) / eks
+    ext["cascade_extend"] = {
+        "call": "minisgl_cascade_extend_attn (prefix pass of all new tokens over the shared rows, "
+                "then each request's own rows with the prefix partial folded in)",
+        "shared_len": P, "value": round(fl / (c_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "ms_per_pass": round(c_ms, 4), "relative_to_extend": round(ext_ms_per_pass / c_ms, 4),
+        "faster": "cascade extend" if c_ms < ext_ms_per_pass else "extend",
+        "l2": "flushed (256 MB write) before each batch's store_kv + timed call"}
+    del cws
     # fused RoPE + store_kv over the same batches (the step before attention)
     max_pos = max(int((b.cached_lens + b.extend_lens).max()) for b in ecase.batches)
     table = workloads.rope_cos_sin_cache(ecase.head_dim, max_pos).to(dev)
@@ -620,7 +696,7 @@ def secondary_objects(mk, args, dev, stream, peaks, st_ms=None, B=None, st_b=Non
     if "tiny" in parts:
         extras["tiny_decode_latency"] = bench_tiny(mk, args, dev, stream)
     if "store_kv" in parts:
-        extras["store_kv"] = bench_store_kv_at_scale(mk, args, dev, stream, peaks, flush)
+        extras["store_kv"] = bench_store_kv_at_scale(mk, args, dev, stream, peaks)
         if st_ms is not None:
             extras["store_kv"]["headline_layer_store"] = {
                 "tokens": B, "ms_per_launch": round(st_ms, 5),

@@ -10,6 +10,7 @@
  *   minisgl_extend_attn  causal attention for the new tokens of chunked prefill
  *   minisgl_rope_store_kv  rotary position embedding of q and k fused with store_kv
  *   minisgl_cascade_decode_attn  decode for requests sharing a prefix, prefix read once
+ *   minisgl_cascade_extend_attn  extend for requests sharing a prefix, prefix pass + own rows
  *
  * Sources of the definitions (page title, section):
  *   [deep-dive]  "mini-sglang 架构深度解读" (mini-sglang architecture deep dive,
@@ -31,10 +32,13 @@
  *     statically sized device memory: the 32 MiB scratch array of
  *     minisgl_decode_attn_noalloc, and 64 work-ticket counters that
  *     minisgl_extend_attn uses to hand out work items to its thread blocks
- *     (each call draws one of the 64 in turn and leaves it at zero when its
- *     kernel completes, so more than 64 extend calls in flight at the same
- *     time on unordered streams would share counters and give wrong
- *     results).
+ *     when the caller passes no counter of its own (each such call draws one
+ *     of the 64 in turn and leaves it at zero when its kernel completes, so
+ *     more than 64 such calls in flight at the same time on unordered
+ *     streams would share counters and give wrong results; callers that run
+ *     extend calls concurrently pass their own counters).  Per device it
+ *     also creates, on first use, one CUDA stream and two events that
+ *     minisgl_cascade_decode_attn uses to run its two parts side by side.
  *   - Element type is bf16 for K, V, Q and the output (MINISGL_BF16); index
  *     tensors are int32.  Strides are in elements.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -197,15 +201,21 @@ int minisgl_store_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const 
  * page_table: as for decode; pt_width columns per row.
  * out: device bf16 [total_q_tokens, num_q_heads, head_dim].
  * sm_scale must be positive and finite (MINISGL_ERR_ARG otherwise).
+ * work_counter: optional device uint32[2], 8-byte aligned, zero before its
+ *   first use; the kernel hands out work items to its thread blocks from it
+ *   and leaves it at zero when it completes.  Calls that may run at the same
+ *   time (unordered streams) need different counters; calls ordered on one
+ *   stream may share one.  NULL: one of the library's 64 slots (see above).
  * Runs on the tensor cores (tcgen05, accumulators in tensor memory).
- * Supported: head_dim 128; num_q_heads/num_kv_heads in {1, 2, 4, 8, 16};
+ * Supported: head_dim 64 or 128; num_q_heads/num_kv_heads any of 1..16;
  * batch <= 4096.
  */
 int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
                         int32_t num_q_heads, const int32_t *page_table, int32_t batch,
                         int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
                         const int32_t *extend_lens, const int32_t *q_offsets,
-                        int32_t total_q_tokens, float sm_scale, void *out, void *stream);
+                        int32_t total_q_tokens, float sm_scale, void *out, uint32_t *work_counter,
+                        void *stream);
 
 /*
  * Workspace size, in bytes, for minisgl_cascade_decode_attn with this batch
@@ -229,11 +239,23 @@ size_t minisgl_cascade_workspace_bytes(int32_t batch, int32_t num_q_heads, int32
  * head for the whole batch instead of once per request: the P prefix
  * positions are attended by all B*G query rows of a KV head at once on the
  * tensor cores (in chunks spread over the SMs), each request's own positions
- * [P, seq_len) by the split-KV decode kernels, and the parts are merged by
- * their log-sum-exp.
+ * [P, seq_len) by the split-KV decode partial kernel, and the parts are
+ * merged by their log-sum-exp in fp32.  When the prefix part leaves at
+ * least 24 SMs free, the suffix part runs on those SMs at the same time, on
+ * a library-owned second stream forked from `stream` and joined back to it
+ * with events (so the call stays capturable in a CUDA graph); otherwise the
+ * parts run one after the other on `stream`.  The library's second stream
+ * is shared by all calls on a device, so two cascade calls on different
+ * caller streams serialise their suffix parts.
  * workspace: device, 256-byte aligned, at least
- *   minisgl_cascade_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim) bytes.
- * Supported: head_dim 128; num_q_heads/num_kv_heads in {1, 2, 4, 8, 16};
+ *   minisgl_cascade_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim)
+ *   bytes.  Its first 256 bytes hold a work counter that must be zero before
+ *   the workspace's first use (every call leaves it at zero); calls that may
+ *   run at the same time need different workspaces.
+ * Cascade pays when the shared prefix dominates the batch's bytes; with
+ * short prefixes its fixed costs (three kernels, the fp32 partials) exceed
+ * the re-read it saves and plain minisgl_decode_attn is faster.
+ * Supported: head_dim 64 or 128; num_q_heads/num_kv_heads any of 1..16;
  * 1 <= shared_len <= pt_width; batch <= 4096.
  */
 int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
@@ -241,6 +263,46 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
                                 int64_t pt_row_stride, int32_t pt_width, const int32_t *seq_lens,
                                 int32_t shared_len, float sm_scale, void *out, void *workspace,
                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Workspace size, in bytes, for minisgl_cascade_extend_attn (an fp32 partial
+ * output row and LSE per new token and query head, and a work counter); 0
+ * for invalid sizes.
+ */
+size_t minisgl_cascade_extend_workspace_bytes(int32_t total_q_tokens, int32_t num_q_heads,
+                                              int32_t head_dim);
+
+/*
+ * Extend attention for a chunked-prefill batch whose requests share a cached
+ * prefix [learn, radix-cache chapter; chunked-prefill chapter; request-state
+ * passage].  Same definition, arguments and result as minisgl_extend_attn,
+ * plus shared_len = P: the caller guarantees that the first P page-table
+ * entries are the same physical rows in every row of the batch and that
+ * every cached_lens[r] >= P (results are unspecified otherwise; nothing is
+ * checked on the device).  Two tensor-core passes: (1) every new token of the
+ * batch against the P shared positions as one block, read once per KV head,
+ * leaving fp32 partial rows and LSEs in the workspace; (2) each request's own
+ * positions P .. C+t causally, with the partial from (1) folded in by
+ * log-sum-exp before the bf16 output is written.
+ * workspace: device, 256-byte aligned, at least
+ *   minisgl_cascade_extend_workspace_bytes(total_q_tokens, num_q_heads, head_dim)
+ *   bytes; its first 256 bytes hold a work counter that must be zero before
+ *   the workspace's first use (every call leaves it at zero); calls that may
+ *   run at the same time need different workspaces.
+ * The new tokens' scores against the shared positions are computed exactly
+ * as often as in minisgl_extend_attn (every token sees every shared
+ * position), so the work is the same; the benefit is the shared K/V tiles
+ * being gathered once per block of 2*floor(128/G) tokens of the whole batch,
+ * at the price of the fp32 partial written and read back (8*d + 8 bytes per
+ * token and query head).
+ * Supported: as minisgl_extend_attn; 1 <= shared_len <= pt_width.
+ */
+int minisgl_cascade_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                                int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                                int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
+                                const int32_t *extend_lens, const int32_t *q_offsets,
+                                int32_t total_q_tokens, int32_t shared_len, float sm_scale, void *out,
+                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Rotary position embedding fused with store_kv [deep-dive 7.3 RoPE: a

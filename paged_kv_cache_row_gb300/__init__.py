@@ -28,7 +28,8 @@ __all__ = [
     "kv_pool_bytes", "load_library", "MinisglError", "EXPORTED_SYMBOLS",
     "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv", "minisgl_cascade_decode_attn",
     "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn", "minisgl_check_indices",
-    "minisgl_debug_set_pdl",
+    "minisgl_debug_set_pdl", "extend_work_counter", "minisgl_cascade_extend_attn",
+    "minisgl_cascade_extend_workspace_bytes",
 ]
 
 EXPORTED_SYMBOLS = [
@@ -36,7 +37,8 @@ EXPORTED_SYMBOLS = [
     "minisgl_extend_attn", "minisgl_last_error", "minisgl_device_sm_count",
     "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
     "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
-    "minisgl_check_indices", "minisgl_debug_set_pdl",
+    "minisgl_check_indices", "minisgl_debug_set_pdl", "minisgl_cascade_extend_attn",
+    "minisgl_cascade_extend_workspace_bytes",
 ]
 
 MINISGL_BF16 = 1
@@ -78,7 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_decode_attn.restype = ctypes.c_int
     lib.minisgl_decode_attn_noalloc.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, f32, vp, i32, vp]
     lib.minisgl_decode_attn_noalloc.restype = ctypes.c_int
-    lib.minisgl_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, f32, vp, vp]
+    lib.minisgl_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, f32, vp, vp,
+                                        vp]
     lib.minisgl_extend_attn.restype = ctypes.c_int
     lib.minisgl_rope_store_kv.argtypes = [P, i32, vp, i32, i64, vp, vp, i64, i64, vp, vp, i32, vp,
                                           i32, vp]
@@ -99,6 +102,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_device_sm_count.restype = i32
     lib.minisgl_debug_timeout_count.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.minisgl_debug_timeout_count.restype = ctypes.c_int
+    lib.minisgl_cascade_extend_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.minisgl_cascade_extend_workspace_bytes.restype = sz
+    lib.minisgl_cascade_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, i32,
+                                                f32, vp, vp, sz, vp]
+    lib.minisgl_cascade_extend_attn.restype = ctypes.c_int
     lib.minisgl_debug_set_pdl.argtypes = [ctypes.c_int]
     lib.minisgl_debug_set_pdl.restype = ctypes.c_int
     _lib = lib
@@ -266,8 +274,12 @@ def minisgl_decode_attn_noalloc(pool: KVPool, layer: int, q: torch.Tensor, page_
 def minisgl_extend_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: torch.Tensor,
                         cached_lens: torch.Tensor, extend_lens: torch.Tensor,
                         q_offsets: torch.Tensor, sm_scale: float,
-                        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Causal extend attention of the packed new tokens q [T, H_q, d]."""
+                        out: Optional[torch.Tensor] = None, work_counter: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Causal extend attention of the packed new tokens q [T, H_q, d].
+    work_counter: optional int32 CUDA tensor of 2 elements, zero before its
+    first use (see extend_work_counter); calls that may run concurrently on
+    different streams need different counters."""
     lib = load_library()
     _need(q, "q", torch.bfloat16)
     for t, nm in ((page_table, "page_table"), (cached_lens, "cached_lens"),
@@ -284,11 +296,20 @@ def minisgl_extend_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: t
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16)
+    if work_counter is not None:
+        _need(work_counter, "work_counter", torch.int32)
+        if work_counter.numel() < 2 or not work_counter.is_contiguous():
+            raise MinisglError("work_counter must be a contiguous int32 tensor of 2 elements")
     _check(lib.minisgl_extend_attn(ctypes.byref(pool.desc), layer, _ptr(q), Hq, _ptr(page_table), B,
                                    page_table.stride(0), page_table.shape[1], _ptr(cached_lens),
                                    _ptr(extend_lens), _ptr(q_offsets), T, float(sm_scale), _ptr(out),
-                                   _stream(stream)), "extend_attn")
+                                   _ptr(work_counter), _stream(stream)), "extend_attn")
     return out
+
+
+def extend_work_counter(device=None) -> torch.Tensor:
+    """A zeroed work counter for minisgl_extend_attn (8 bytes of device memory)."""
+    return torch.zeros(2, dtype=torch.int32, device=device or "cuda")
 
 
 def minisgl_device_sm_count() -> int:
@@ -401,7 +422,8 @@ def minisgl_cascade_decode_attn(pool: KVPool, layer: int, q: torch.Tensor, page_
         key = ("cascade", q.device, nbytes)
         workspace = _ws_cache.get(key)
         if workspace is None:
-            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+            # the first 256 bytes (a work counter) must start at zero
+            workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
             _ws_cache[key] = workspace
     _check(lib.minisgl_cascade_decode_attn(ctypes.byref(pool.desc), layer, _ptr(q), Hq, _ptr(page_table),
                                            B, page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
@@ -445,4 +467,50 @@ def minisgl_store_decode_attn(pool: KVPool, layer: int, k: torch.Tensor, v: torc
                                          page_table.stride(0), page_table.shape[1], _ptr(seq_lens),
                                          float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
                                          split_tokens, _stream(stream)), "store_decode_attn")
+    return out
+
+
+def minisgl_cascade_extend_workspace_bytes(total_q_tokens: int, num_q_heads: int, head_dim: int) -> int:
+    return int(load_library().minisgl_cascade_extend_workspace_bytes(total_q_tokens, num_q_heads,
+                                                                     head_dim))
+
+
+def minisgl_cascade_extend_attn(pool: KVPool, layer: int, q: torch.Tensor, page_table: torch.Tensor,
+                                cached_lens: torch.Tensor, extend_lens: torch.Tensor,
+                                q_offsets: torch.Tensor, shared_len: int, sm_scale: float,
+                                out: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal extend attention of q [T, H_q, d] for requests whose first
+    shared_len page-table entries are the same rows: a pass of all new tokens
+    against the shared rows, then each request's own rows with that pass's
+    partial folded in."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16)
+    for t, nm in ((page_table, "page_table"), (cached_lens, "cached_lens"),
+                  (extend_lens, "extend_lens"), (q_offsets, "q_offsets")):
+        _need(t, nm, torch.int32)
+    T, Hq, d = q.shape
+    B = cached_lens.numel()
+    if not q.is_contiguous() or d != pool.head_dim:
+        raise MinisglError("q must be contiguous [T, H_q, head_dim]")
+    if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if extend_lens.numel() != B or q_offsets.numel() != B + 1:
+        raise MinisglError("extend_lens must be [B] and q_offsets [B+1]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16)
+    if workspace is None:
+        nbytes = minisgl_cascade_extend_workspace_bytes(T, Hq, d)
+        key = ("cascade_extend", q.device, nbytes)
+        workspace = _ws_cache.get(key)
+        if workspace is None:
+            # the first 256 bytes (a work counter) must start at zero
+            workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+            _ws_cache[key] = workspace
+    _check(lib.minisgl_cascade_extend_attn(ctypes.byref(pool.desc), layer, _ptr(q), Hq, _ptr(page_table), B,
+                                           page_table.stride(0), page_table.shape[1], _ptr(cached_lens),
+                                           _ptr(extend_lens), _ptr(q_offsets), T, int(shared_len),
+                                           float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                           _stream(stream)), "cascade_extend_attn")
     return out

@@ -295,15 +295,14 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
                         int32_t num_q_heads, const int32_t *page_table, int32_t batch,
                         int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
                         const int32_t *extend_lens, const int32_t *q_offsets,
-                        int32_t total_q_tokens, float sm_scale, void *out, void *stream) {
+                        int32_t total_q_tokens, float sm_scale, void *out, uint32_t *work_counter,
+                        void *stream) {
     g_err.clear();
     NvtxRange nvtx_range("minisgl_extend_attn");
     if (int rc = check_pool(pool, layer, "extend_attn")) return rc;
-    if (pool->head_dim != 128)
-        return fail(MINISGL_ERR_UNSUPPORTED, "extend_attn: head_dim %d (only 128)", pool->head_dim);
     if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "extend_attn")) return rc;
-    const int G = num_q_heads / pool->num_kv_heads;
-    if (G & (G - 1)) return fail(MINISGL_ERR_UNSUPPORTED, "extend_attn: group size %d not a power of 2", G);
+    if (work_counter && (reinterpret_cast<uintptr_t>(work_counter) & 7u))
+        return fail(MINISGL_ERR_ARG, "extend_attn: work_counter must be 8-byte aligned");
     if (batch < 0 || batch > 4096) return fail(MINISGL_ERR_ARG, "extend_attn: batch %d outside [0, 4096]", batch);
     if (total_q_tokens < 0) return fail(MINISGL_ERR_ARG, "extend_attn: total_q_tokens < 0");
     if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f))
@@ -338,6 +337,7 @@ int minisgl_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *
     a.out_f32 = nullptr;
     a.lse_out = nullptr;
     a.out_offsets = nullptr;
+    a.sched = work_counter;
     return cuda_status(minisgl::launch_extend(a, static_cast<cudaStream_t>(stream)), "extend_attn");
 }
 
@@ -350,11 +350,12 @@ constexpr int CASCADE_MAX_CHUNKS = 32;
 constexpr int CASCADE_SUFFIX_SPLITS = 16;
 
 // Workspace layout of minisgl_cascade_decode_attn (each part 256-byte aligned):
-// int32 metadata (4 arrays of chunks+1, one of batch), fp32 prefix partials
-// [chunks, B, Hq, D] and their LSEs [chunks, B, Hq], the bf16 suffix result
-// [B, Hq, D] and its LSEs [B, Hq], then a decode workspace for the suffix.
+// the prefix launch's work-ticket counter (8 bytes in a 256-byte part), fp32
+// prefix partials [chunks, B, Hq, D] and their LSEs [chunks, B, Hq], then a
+// decode workspace for the suffix's split partials.
 // Most prefix chunks a call with this shape uses: about two work items per
-// SM (a work item covers 2*128/G query rows of one KV head), at most 32.
+// SM (a work item covers 2*floor(128/G) query tokens of one KV head), at
+// most 32.
 int64_t cascade_chunk_cap(int64_t batch, int64_t hq, int64_t hkv) {
     const int64_t g = std::max<int64_t>(1, hq / hkv);
     const int64_t tq2 = std::max<int64_t>(1, 2 * (128 / g));
@@ -365,9 +366,7 @@ int64_t cascade_chunk_cap(int64_t batch, int64_t hq, int64_t hkv) {
 }
 
 size_t cascade_bytes(int64_t batch, int64_t hq, int64_t hkv, int64_t d, int64_t chunks) {
-    return align256((size_t)(4 * (chunks + 1) + batch) * 4) +
-           align256((size_t)chunks * batch * hq * d * 4) + align256((size_t)chunks * batch * hq * 4) +
-           align256((size_t)batch * hq * d * 2) + align256((size_t)batch * hq * 4) +
+    return 256 + align256((size_t)chunks * batch * hq * d * 4) + align256((size_t)chunks * batch * hq * 4) +
            ws_bytes(batch, hq, hkv, d, CASCADE_SUFFIX_SPLITS);
 }
 
@@ -390,12 +389,7 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
     g_err.clear();
     NvtxRange nvtx_range("minisgl_cascade_decode_attn");
     if (int rc = check_pool(pool, layer, "cascade_decode_attn")) return rc;
-    if (pool->head_dim != 128)
-        return fail(MINISGL_ERR_UNSUPPORTED, "cascade_decode_attn: head_dim %d (only 128)", pool->head_dim);
     if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "cascade_decode_attn")) return rc;
-    const int G = num_q_heads / pool->num_kv_heads;
-    if (G & (G - 1))
-        return fail(MINISGL_ERR_UNSUPPORTED, "cascade_decode_attn: group size %d not a power of 2", G);
     if (batch < 0 || batch > 4096)
         return fail(MINISGL_ERR_ARG, "cascade_decode_attn: batch %d outside [0, 4096]", batch);
     if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f))
@@ -420,63 +414,65 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
     if (workspace_bytes < need)
         return fail(MINISGL_ERR_WORKSPACE, "cascade_decode_attn: workspace %zu bytes < %zu", workspace_bytes,
                     need);
-    minisgl::ExtendArgs base;
-    base.q = q;
-    base.k_layer = layer_ptr(pool->k_base, pool, layer);
-    base.v_layer = layer_ptr(pool->v_base, pool, layer);
-    base.row_stride = pool->row_stride;
-    base.num_rows = pool->num_rows;
-    base.num_q_heads = num_q_heads;
-    base.num_kv_heads = pool->num_kv_heads;
-    base.head_dim = pool->head_dim;
-    base.sm_scale = sm_scale;
-    base.out = nullptr;
-    minisgl::CascadeArgs c;
     char *ws = static_cast<char *>(workspace);
-    int32_t *meta = reinterpret_cast<int32_t *>(ws);
-    const int64_t S1 = chunks + 1;
-    c.meta.pre_cached = meta;
-    c.meta.pre_extend = meta + S1;
-    c.meta.pre_qoff = meta + 2 * S1;
-    c.meta.pre_ooff = meta + 3 * S1;
-    c.meta.suf_seq = meta + 4 * S1;
-    ws += align256((size_t)(4 * S1 + batch) * 4);
+    // prefix: chunk c is positions [c*chunk_len, ...) of the shared rows, read
+    // from the first page-table row; every chunk reads q rows 0..B-1
+    minisgl::ExtendArgs p;
+    p.q = q;
+    p.k_layer = layer_ptr(pool->k_base, pool, layer);
+    p.v_layer = layer_ptr(pool->v_base, pool, layer);
+    p.row_stride = pool->row_stride;
+    p.num_rows = pool->num_rows;
+    p.page_table = page_table;
+    p.pt_stride = chunk_len;
+    p.pt_width = (int32_t)chunk_len;
+    p.cached_lens = p.extend_lens = p.q_offsets = nullptr;
+    p.batch = (int32_t)chunks;
+    p.total_q_tokens = (int32_t)(chunks * batch);
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.head_dim = pool->head_dim;
+    p.sm_scale = sm_scale;
+    p.out = nullptr;
+    p.prefix_only = 1;
+    p.out_offsets = nullptr;
+    p.prefix_chunk_len = (int32_t)chunk_len;
+    p.prefix_len = shared_len;
+    p.prefix_queries = batch;
+    p.sched = reinterpret_cast<unsigned int *>(ws);
+    ws += 256;
     const size_t vec = (size_t)batch * num_q_heads;
+    minisgl::CascadeArgs c;
     c.pre_o = reinterpret_cast<float *>(ws);
     ws += align256((size_t)chunks * vec * d * 4);
     c.pre_lse = reinterpret_cast<float *>(ws);
     ws += align256((size_t)chunks * vec * 4);
-    c.suf_out = ws;
-    ws += align256(vec * d * 2);
-    c.suf_lse = reinterpret_cast<float *>(ws);
-    ws += align256(vec * 4);
-    c.page_table = page_table;
-    c.pt_row_stride = pt_row_stride;
-    c.pt_width = pt_width;
+    p.out_f32 = c.pre_o;
+    p.lse_out = c.pre_lse;
     c.seq_lens = seq_lens;
     c.batch = batch;
     c.num_q_heads = num_q_heads;
     c.head_dim = pool->head_dim;
     c.shared_len = shared_len;
     c.chunks = (int32_t)chunks;
-    c.chunk_len = (int32_t)chunk_len;
     c.out = out;
     minisgl::DecodeArgs &sd = c.suffix;  // the suffix: page table shifted by P columns
     sd.q = q;
-    sd.k_layer = base.k_layer;
-    sd.v_layer = base.v_layer;
+    sd.k_layer = p.k_layer;
+    sd.v_layer = p.v_layer;
     sd.row_stride = pool->row_stride;
     sd.num_rows = pool->num_rows;
     sd.page_table = page_table + shared_len;
     sd.pt_stride = pt_row_stride;
     sd.pt_width = pt_width - shared_len;
-    sd.seq_lens = c.meta.suf_seq;
+    sd.seq_lens = seq_lens;
+    sd.len_offset = shared_len;
     sd.batch = batch;
     sd.num_q_heads = num_q_heads;
     sd.num_kv_heads = pool->num_kv_heads;
     sd.head_dim = pool->head_dim;
     sd.sm_scale = sm_scale;
-    sd.out = c.suf_out;
+    sd.out = nullptr;
     sd.split_count = reinterpret_cast<int32_t *>(ws);
     ws += align256((size_t)batch * Hkv * 4);
     sd.ws_lse = reinterpret_cast<float *>(ws);
@@ -484,12 +480,102 @@ int minisgl_cascade_decode_attn(const minisgl_kv_pool *pool, int32_t layer, cons
     sd.ws_o = reinterpret_cast<float *>(ws);
     sd.max_splits = CASCADE_SUFFIX_SPLITS;
     sd.split_tokens = 0;
-    sd.lse_out = c.suf_lse;
+    sd.lse_out = nullptr;
     sd.out_loc = nullptr;
     sd.k_new = sd.v_new = nullptr;
     sd.new_k_stride = sd.new_v_stride = 0;
-    return cuda_status(minisgl::launch_cascade(c, base, static_cast<cudaStream_t>(stream)),
+    sd.partials_only = 1;
+    return cuda_status(minisgl::launch_cascade(c, p, static_cast<cudaStream_t>(stream)),
                        "cascade_decode_attn");
+}
+
+size_t minisgl_cascade_extend_workspace_bytes(int32_t total_q_tokens, int32_t num_q_heads,
+                                              int32_t head_dim) {
+    if (total_q_tokens < 0 || num_q_heads < 1 || head_dim < 1) return 0;
+    const size_t rows = (size_t)total_q_tokens * num_q_heads;
+    return 256 + align256(rows * head_dim * 4) + align256(rows * 4);
+}
+
+int minisgl_cascade_extend_attn(const minisgl_kv_pool *pool, int32_t layer, const void *q,
+                                int32_t num_q_heads, const int32_t *page_table, int32_t batch,
+                                int64_t pt_row_stride, int32_t pt_width, const int32_t *cached_lens,
+                                const int32_t *extend_lens, const int32_t *q_offsets,
+                                int32_t total_q_tokens, int32_t shared_len, float sm_scale, void *out,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    g_err.clear();
+    NvtxRange nvtx_range("minisgl_cascade_extend_attn");
+    if (int rc = check_pool(pool, layer, "cascade_extend_attn")) return rc;
+    if (int rc = check_heads(num_q_heads, pool->num_kv_heads, 16, "cascade_extend_attn")) return rc;
+    if (batch < 0 || batch > 4096)
+        return fail(MINISGL_ERR_ARG, "cascade_extend_attn: batch %d outside [0, 4096]", batch);
+    if (total_q_tokens < 0) return fail(MINISGL_ERR_ARG, "cascade_extend_attn: total_q_tokens < 0");
+    if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f))
+        return fail(MINISGL_ERR_ARG, "cascade_extend_attn: sm_scale must be positive and finite");
+    if (pt_width < 1 || pt_row_stride < pt_width)
+        return fail(MINISGL_ERR_SHAPE, "cascade_extend_attn: need 1 <= pt_width <= pt_row_stride");
+    if (shared_len < 1 || shared_len > pt_width)
+        return fail(MINISGL_ERR_ARG, "cascade_extend_attn: shared_len %d outside [1, pt_width]", shared_len);
+    if (batch == 0 || total_q_tokens == 0) return MINISGL_OK;
+    if (!q || !page_table || !cached_lens || !extend_lens || !q_offsets || !out || !workspace)
+        return fail(MINISGL_ERR_ARG, "cascade_extend_attn: NULL pointer argument");
+    if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MINISGL_ERR_SHAPE, "cascade_extend_attn: q, out 16-byte and workspace 256-byte aligned");
+    const size_t need = minisgl_cascade_extend_workspace_bytes(total_q_tokens, num_q_heads, pool->head_dim);
+    if (workspace_bytes < need)
+        return fail(MINISGL_ERR_WORKSPACE, "cascade_extend_attn: workspace %zu bytes < %zu", workspace_bytes,
+                    need);
+    char *ws = static_cast<char *>(workspace);
+    const size_t rows = (size_t)total_q_tokens * num_q_heads;
+    unsigned int *counter = reinterpret_cast<unsigned int *>(ws);
+    float *pre_o = reinterpret_cast<float *>(ws + 256);
+    float *pre_lse = reinterpret_cast<float *>(ws + 256 + align256(rows * pool->head_dim * 4));
+    // the new tokens' common part: all of them against the P shared positions,
+    // one pseudo-request whose page-table row is the first request's
+    minisgl::ExtendArgs p;
+    p.q = q;
+    p.k_layer = layer_ptr(pool->k_base, pool, layer);
+    p.v_layer = layer_ptr(pool->v_base, pool, layer);
+    p.row_stride = pool->row_stride;
+    p.num_rows = pool->num_rows;
+    p.page_table = page_table;
+    p.pt_stride = shared_len;
+    p.pt_width = shared_len;
+    p.cached_lens = p.extend_lens = p.q_offsets = nullptr;
+    p.batch = 1;
+    p.total_q_tokens = total_q_tokens;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.head_dim = pool->head_dim;
+    p.sm_scale = sm_scale;
+    p.out = nullptr;
+    p.prefix_only = 1;
+    p.out_f32 = pre_o;
+    p.lse_out = pre_lse;
+    p.out_offsets = nullptr;
+    p.prefix_chunk_len = shared_len;
+    p.prefix_len = shared_len;
+    p.prefix_queries = total_q_tokens;
+    p.sched = counter;
+    // each request's own positions, causally, with the common part folded in
+    minisgl::ExtendArgs o = p;
+    o.page_table = page_table + shared_len;
+    o.pt_stride = pt_row_stride;
+    o.pt_width = pt_width - shared_len;
+    o.cached_lens = cached_lens;
+    o.extend_lens = extend_lens;
+    o.q_offsets = q_offsets;
+    o.batch = batch;
+    o.out = out;
+    o.prefix_only = 0;
+    o.out_f32 = nullptr;
+    o.lse_out = nullptr;
+    o.prefix_chunk_len = o.prefix_len = o.prefix_queries = 0;
+    o.len_offset = shared_len;
+    o.merge_o = pre_o;
+    o.merge_lse = pre_lse;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (int rc = cuda_status(minisgl::launch_extend(p, st), "cascade_extend_attn")) return rc;
+    return cuda_status(minisgl::launch_extend(o, st), "cascade_extend_attn");
 }
 
 int minisgl_rope_store_kv(const minisgl_kv_pool *pool, int32_t layer, void *q, int32_t num_q_heads,

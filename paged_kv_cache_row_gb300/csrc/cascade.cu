@@ -12,18 +12,21 @@
 //   * prefix: all B decode queries against positions [0, P) of the shared
 //     rows.  That is a dense multi-query block -- for KV head g, B*G query
 //     rows against the same keys -- so it runs on the tensor cores in the
-//     extend kernel's prefix-only mode: one pseudo-request per chunk of the
-//     prefix (its page-table row starts at the chunk's first column, so the
-//     row stride is the chunk length), all of them reading q rows 0..B-1 and
-//     writing fp32 partial outputs and LSEs to their own rows.  Chunks are
-//     sized so the launch has about two work items per SM.
+//     extend kernel's prefix-chunk mode: chunk c covers shared positions
+//     [c*chunk_len, (c+1)*chunk_len) of the first page-table row, every chunk
+//     reads q rows 0..B-1 and writes fp32 partial outputs and LSEs to its own
+//     rows.  The chunk geometry is arithmetic, so no metadata is written.
 //   * suffix: each request's own positions [P, n_r) with the split-KV decode
-//     kernels (page table shifted by P columns, context n_r - P), which also
-//     return each row's LSE.
-//   * merge: per (request, query head), the prefix chunks and the suffix are
-//     combined by their LSEs and written as bf16.
-// A setup kernel writes the pseudo-requests' lengths and offsets into the
-// caller's workspace, so the call allocates nothing and never synchronises.
+//     partial kernel (page table shifted by P columns, context n_r - P),
+//     which leaves fp32 partials and LSEs for every stream, split or not.
+//   * merge: per (request, query head), the prefix chunks and the suffix
+//     splits are combined by their LSEs in fp32 and written as bf16.
+// The two parts are independent.  When the prefix launch leaves enough SMs
+// free, the suffix runs on a library-owned second stream, forked from and
+// joined back to the caller's stream with events (capturable in a CUDA
+// graph), on those free SMs only, so both parts run at the same time.
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -31,58 +34,52 @@ namespace minisgl {
 
 namespace {
 
-// pseudo-request metadata of the prefix launch and the suffix lengths
-__global__ void cascade_setup_kernel(CascadeArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int B = a.batch, S = a.chunks;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B + S + 1; i += gridDim.x * blockDim.x) {
-        if (i < S) {  // prefix chunk i
-            a.meta.pre_cached[i] = min(a.chunk_len, a.shared_len - i * a.chunk_len);
-            a.meta.pre_extend[i] = B;
-            a.meta.pre_qoff[i] = 0;
-            a.meta.pre_ooff[i] = i * B;
-        } else if (i < S + B) {  // suffix of request r
-            const int r = i - S;
-            a.meta.suf_seq[r] = max(__ldg(a.seq_lens + r) - a.shared_len, 0);
-        } else {
-            a.meta.pre_qoff[S] = B;
-        }
-    }
-}
-
-// one warp per (request, query head): merge the S prefix partials (fp32) and
-// the suffix result (bf16, weight 0 when its LSE is -inf: empty suffix)
+// one warp per (request, query head): merge the prefix chunks' fp32 partials
+// (lane c holds chunk c's LSE) and the suffix's split partials (lane s holds
+// split s's LSE; none when the request has no private positions)
 template <int D>
 __global__ void __launch_bounds__(256) cascade_merge_kernel(CascadeArgs a) {
     pdl_wait();
     pdl_launch_dependents();
     constexpr int PER = D / 32;  // channels per lane
     const int lane = threadIdx.x & 31;
+    const DecodeArgs &sd = a.suffix;
+    const int G = a.num_q_heads / sd.num_kv_heads;
     const int64_t nvec = (int64_t)a.batch * a.num_q_heads;
     for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < nvec;
          v += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-        // lane p < S holds prefix chunk p's LSE
+        const int r = (int)(v / a.num_q_heads), h = (int)(v - (int64_t)r * a.num_q_heads);
+        const int n_suf = min(max(__ldg(a.seq_lens + r) - a.shared_len, 0), sd.pt_width);
+        const int S = n_suf > 0 ? min(sd.split_count[(int64_t)r * sd.num_kv_heads + h / G], sd.max_splits) : 0;
+        const int64_t sbase = v * sd.max_splits;
         const float lp = lane < a.chunks ? a.pre_lse[(int64_t)lane * nvec + v] : -INFINITY;
-        const float ls = a.suf_lse[v];
+        const float ls = lane < S ? sd.ws_lse[sbase + lane] : -INFINITY;
         float top = fmaxf(lp, ls);
 #pragma unroll
         for (int o = 16; o; o >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
         const float wp = lane < a.chunks ? __expf(lp - top) : 0.f;
-        const float ws = ls == -INFINITY ? 0.f : __expf(ls - top);
-        float total = wp;
+        const float ws = lane < S ? __expf(ls - top) : 0.f;
+        float total = wp + ws;
 #pragma unroll
         for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-        total += ws;
         float acc[PER];
-        {
-            const __nv_bfloat16 *so = static_cast<const __nv_bfloat16 *>(a.suf_out) + v * D + lane * PER;
 #pragma unroll
-            for (int c = 0; c < PER; ++c) acc[c] = ws * __bfloat162float(so[c]);
-        }
+        for (int c = 0; c < PER; ++c) acc[c] = 0.f;
         for (int p = 0; p < a.chunks; ++p) {
             const float w = __shfl_sync(0xffffffffu, wp, p);
             const float *o = a.pre_o + ((int64_t)p * nvec + v) * D + lane * PER;
+#pragma unroll
+            for (int c = 0; c < PER; c += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(o + c);
+                acc[c] += w * x.x;
+                acc[c + 1] += w * x.y;
+                acc[c + 2] += w * x.z;
+                acc[c + 3] += w * x.w;
+            }
+        }
+        for (int s = 0; s < S; ++s) {
+            const float w = __shfl_sync(0xffffffffu, ws, s);
+            const float *o = sd.ws_o + (sbase + s) * D + lane * PER;
 #pragma unroll
             for (int c = 0; c < PER; c += 4) {
                 const float4 x = *reinterpret_cast<const float4 *>(o + c);
@@ -100,34 +97,69 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(CascadeArgs a) {
     }
 }
 
+// A second stream per device and the two events that fork work onto it and
+// join it back, created on first use.  The mutex is held while a call
+// enqueues its fork, its side-stream launch and its join, so calls from
+// several host threads do not interleave their uses of the events.
+struct Side {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+Side g_side[64];
+
+cudaError_t side_for_current_device(Side **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    Side &sd = g_side[dev];
+    if (!sd.stream) {
+        if ((e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &sd;
+    return cudaSuccess;
+}
+
+// SMs the suffix needs at least before it is worth running beside the prefix
+constexpr int MIN_FREE_SMS = 24;
+
 }  // namespace
 
-cudaError_t launch_cascade(const CascadeArgs &c, const ExtendArgs &base, cudaStream_t s) {
+cudaError_t launch_cascade(const CascadeArgs &c, const ExtendArgs &prefix, cudaStream_t s) {
     if (c.batch == 0) return cudaSuccess;
-    cudaError_t e = launch_pdl(cascade_setup_kernel, dim3(1), dim3(256), 0, s, c);
-    if (e != cudaSuccess) return e;
-    // prefix: one pseudo-request per chunk, rows of the shared prefix
-    ExtendArgs p = base;
-    p.page_table = c.page_table;
-    p.pt_stride = c.chunk_len;
-    p.pt_width = c.chunk_len;
-    p.batch = c.chunks;
-    p.total_q_tokens = c.chunks * c.batch;
-    p.cached_lens = c.meta.pre_cached;
-    p.extend_lens = c.meta.pre_extend;
-    p.q_offsets = c.meta.pre_qoff;
-    p.out_offsets = c.meta.pre_ooff;
-    p.prefix_only = 1;
-    p.out_f32 = c.pre_o;
-    p.lse_out = c.pre_lse;
-    if ((e = launch_extend(p, s)) != cudaSuccess) return e;
-    // suffix: split-KV decode over each request's own positions, with LSEs
-    if ((e = launch_decode(c.suffix, s)) != cudaSuccess) return e;
+    const int sms = device_sm_count();
+    const int free_sms = sms - extend_grid(prefix);
     const int64_t warps = (int64_t)c.batch * c.num_q_heads;
     int64_t blocks = (warps * 32 + 255) / 256;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
-    if (blocks > cap) blocks = cap;
-    return launch_pdl(cascade_merge_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, s, c);
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    auto merge = [&]() {
+        return c.head_dim == 64
+                   ? launch_pdl(cascade_merge_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, s, c)
+                   : launch_pdl(cascade_merge_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, s, c);
+    };
+    cudaError_t e;
+    if (free_sms < MIN_FREE_SMS) {  // one after the other on the caller's stream
+        if ((e = launch_extend(prefix, s)) != cudaSuccess) return e;
+        if ((e = launch_decode(c.suffix, s)) != cudaSuccess) return e;
+        return merge();
+    }
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    Side *side = nullptr;
+    if ((e = side_for_current_device(&side)) != cudaSuccess) return e;
+    // the prefix goes first, so its CTAs take their SMs before the suffix's
+    // are placed; the suffix is limited to the SMs left over
+    if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return e;
+    if ((e = launch_extend(prefix, s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
+    DecodeArgs suf = c.suffix;
+    suf.max_sms = free_sms;
+    if ((e = launch_decode(suf, side->stream)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, side->join, 0)) != cudaSuccess) return e;
+    return merge();
 }
 
 }  // namespace minisgl

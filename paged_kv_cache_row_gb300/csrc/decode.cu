@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
         for (int base = 0; base < B; base += 32) {
             const int r = base + lane;
             int nt = 0;
-            if (r < B) nt = (clamp_len(__ldg(a.seq_lens + r), W) + TILE - 1) / TILE;
+            if (r < B) nt = (clamp_len(__ldg(a.seq_lens + r) - a.len_offset, W) + TILE - 1) / TILE;
             mx = max(mx, nt);
             int v = nt * Hkv;
 #pragma unroll
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
             if (s_prefix[mid] <= t) lo = mid; else hi = mid;
         }
         c.r = lo;
-        c.n = clamp_len(__ldg(a.seq_lens + lo), W);
+        c.n = clamp_len(__ldg(a.seq_lens + lo) - a.len_offset, W);
         c.nt = (c.n + TILE - 1) / TILE;
         const int off = t - s_prefix[lo];
         c.g = off / c.nt;
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
             if (++c.g == Hkv) {
                 c.g = 0;
                 do { ++c.r; } while (s_prefix[c.r + 1] == s_prefix[c.r]);
-                c.n = clamp_len(__ldg(a.seq_lens + c.r), W);
+                c.n = clamp_len(__ldg(a.seq_lens + c.r) - a.len_offset, W);
                 c.nt = (c.n + TILE - 1) / TILE;
             }
         }
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(MAX_WARPS * 32, 1)
                     if (h >= G) continue;
                     const float inv = 1.f / lt;
                     const int64_t hh = (int64_t)cur_r * Hq + cur_g * G + h;
-                    if (whole) {
+                    if (whole && !a.partials_only) {
                         if (a.lse_out && dr == 0) a.lse_out[hh] = (m[n][e] + __log2f(lt)) * LN2;
                         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + hh * D + dr;
 #pragma unroll
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     // by the partial kernel only for non-empty requests, so read after the
     // empty check), then the first 32 LSEs together with the first PRE
     // partial rows
-    const int n = min(max(__ldg(a.seq_lens + r), 0), a.pt_width);
+    const int n = min(max(__ldg(a.seq_lens + r) - a.len_offset, 0), a.pt_width);
     if (n == 0) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) out[c] = __float2bfloat16_rn(0.f);
@@ -598,10 +598,11 @@ cudaError_t launch_cfg(const DecodeArgs &a, cudaStream_t s) {
     int64_t grid = (int64_t)device_sm_count() * nb;
     const int64_t need = (max_tiles + warps - 1) / warps;
     if (grid > need) grid = need;
+    if (a.max_sms > 0 && grid > (int64_t)a.max_sms * nb) grid = (int64_t)a.max_sms * nb;
     if (grid < 1) grid = 1;
     cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(warps * 32), smem, s, a,
                                a.sm_scale * LOG2E, prefix_bytes, stage_bytes);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || a.partials_only) return e;
     return launch_pdl(decode_merge_kernel<D>, dim3((a.batch * a.num_q_heads + 3) / 4), dim3(128), 0,
                       s, a);
 }

@@ -10,11 +10,13 @@
 // 0 .. C_r + t of its page_table row:
 //     out[q_off[r]+t, h] = sum_{j <= C_r+t} softmax_j(sm_scale <q, K[pt[r,j], g]>) V[pt[r,j], g].
 //
-// Design (GB300, one CTA per SM, persistent):
-//   * Work item = (request, KV head g, block of 2*TQ new tokens), TQ = 128/G.
-//     The block is two query tiles A and B of 128 MMA rows each; a row is a
-//     (token, head) pair, so the G query heads that share KV head g ride in
-//     the same tile and every gathered K/V tile feeds 2*128 rows.
+// Design (GB300, one CTA per SM, persistent; head_dim d = 64 or 128):
+//   * Work item = (request, KV head g, block of 2*TQ new tokens), TQ =
+//     floor(128/G) for any group size G = 1..16.  The block is two query
+//     tiles A and B of 128 MMA rows each; row i is the (token i / G, head
+//     i mod G) pair, so the G query heads that share KV head g ride in the
+//     same tile and every gathered K/V tile feeds 2*128 rows (rows past
+//     TQ*G, 2 at most for G in 3, 5, 6, 7, are dead: zero queries, no output).
 //   * Producer warps 8-9 gather 128-token K and V tiles through page_table
 //     with 16-byte cp.async into the 128-byte-swizzled layout the tensor core
 //     reads (K as a K-major B operand, V as an MN-major B operand), two
@@ -42,9 +44,11 @@
 //     P is then at most 2^20, well inside fp32 and bf16 range, and bf16
 //     keeps the same relative precision at any magnitude.
 //     Epilogue: O / l -> bf16 -> global.
-//   * Tensor memory (512 columns): S_A 0-127, S_B 128-255, O_A 256-383,
-//     O_B 384-511.  Shared memory: Q_A, Q_B (32 KB each), two K/V stages
-//     (64 KB each).
+//   * Tensor memory (512 columns): S_A 0-127, S_B 128-255, O_A from 256,
+//     O_B from 384 (d columns each).  Shared memory: Q_A, Q_B (128 rows of
+//     2d bytes each), two K/V stages (two such tiles each): 192 KB at d 128.
+//   * The work-ticket counter of the dynamic schedule is the caller's when
+//     given, else one of 64 library slots taken in turn.
 //   * Every mbarrier wait is bounded in time; a wait that runs out sets a
 //     flag, the kernel finishes without further waiting (its output is then
 //     garbage) and a device counter of such events is increased.
@@ -68,19 +72,23 @@ __device__ SchedSlot g_sched[64];
 
 namespace {
 
-constexpr int D = 128;
 constexpr int ROWS = 128;                 // rows of a query tile, tokens of a KV tile
-constexpr int TILE_BYTES = ROWS * D * 2;  // 32 KB: 128 rows of 256 bytes
-constexpr int HALF = TILE_BYTES / 2;      // one 64-column swizzle region
-constexpr int OFF_Q = 0;                  // Q_A, then Q_B
-constexpr int OFF_KV = 2 * TILE_BYTES;    // stage s: K at +2s*TILE, V at +(2s+1)*TILE
+constexpr int HALF = ROWS * 128;          // one 64-column (128-byte) swizzle region of a tile
 constexpr int STAGES = 2;
-constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE_BYTES;  // 192 KB
-constexpr int OFF_TMEM_SLOT = OFF_BAR + 192;
-constexpr int OFF_RING = OFF_BAR + 256;   // ring of RING work-item descriptors (64 B each)
 constexpr int RING = 8;
-constexpr int OFF_PREFIX = OFF_RING + RING * 64;
 constexpr int SCHED_SLOTS = 64;           // per-call work-ticket counters
+
+// Shared-memory layout for head_dim D
+template <int D>
+struct Smem {
+    static constexpr int TILE_BYTES = ROWS * D * 2;  // 128 rows of 2D bytes
+    static constexpr int OFF_Q = 0;                  // Q_A, then Q_B
+    static constexpr int OFF_KV = 2 * TILE_BYTES;    // stage s: K at +2s*TILE, V at +(2s+1)*TILE
+    static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TILE_BYTES;
+    static constexpr int OFF_TMEM_SLOT = OFF_BAR + 192;
+    static constexpr int OFF_RING = OFF_BAR + 256;   // ring of RING work-item descriptors (64 B each)
+    static constexpr int OFF_PREFIX = OFF_RING + RING * 64;
+};
 constexpr int THREADS = 384;              // 2 softmax warpgroups, 2 producer warps, idle warp, MMA warp
 constexpr int PRODUCER_WARP0 = 8;
 constexpr int PRODUCER_THREADS = 64;
@@ -257,8 +265,23 @@ struct Item {
     __device__ __forceinline__ int n_vis() const { return vis; }
 };
 
+// Cached tokens C and new tokens E of request r: from the length arrays, or,
+// for chunk r of a shared prefix (prefix_chunk_len > 0), from the chunk
+// geometry: C = the chunk's length, E = the prefix_queries decode queries.
+__device__ __forceinline__ void req_lens(const ExtendArgs &a, int r, int &C, int &E) {
+    if (a.prefix_chunk_len > 0) {
+        C = min(a.prefix_chunk_len, a.prefix_len - r * a.prefix_chunk_len);
+        E = a.prefix_queries;
+        return;
+    }
+    C = min(max(__ldg(a.cached_lens + r) - a.len_offset, 0), a.pt_width);
+    // (in prefix-only mode a new token is not a page-table position)
+    E = a.prefix_only ? max(__ldg(a.extend_lens + r), 0)
+                      : min(max(__ldg(a.extend_lens + r), 0), a.pt_width - C);
+}
+
 // Work item `item` from the per-request prefix of item counts in shared
-// memory (binary search) and the request's lengths from global memory.
+// memory (binary search) and the request's lengths.
 __device__ __forceinline__ Item load_item(const ExtendArgs &a, const int32_t *s_prefix, int item,
                                           int TQ) {
     int lo = 0, hi = a.batch;
@@ -272,13 +295,15 @@ __device__ __forceinline__ Item load_item(const ExtendArgs &a, const int32_t *s_
     const int off = item - s_prefix[lo];
     it.g = off / nqb;
     const int qb = off - it.g * nqb;
-    const int W = a.pt_width;
-    it.C = min(max(__ldg(a.cached_lens + lo), 0), W);
-    // (in prefix-only mode a new token is not a page-table position)
-    const int E = a.prefix_only ? max(__ldg(a.extend_lens + lo), 0)
-                                : min(max(__ldg(a.extend_lens + lo), 0), W - it.C);
-    it.qoff = __ldg(a.q_offsets + lo);
-    it.ooff = a.out_offsets ? __ldg(a.out_offsets + lo) : it.qoff;
+    int E;
+    req_lens(a, lo, it.C, E);
+    if (a.prefix_chunk_len > 0) {  // every chunk reads q rows 0.. and writes its own rows
+        it.qoff = 0;
+        it.ooff = lo * a.prefix_queries;
+    } else {
+        it.qoff = __ldg(a.q_offsets + lo);
+        it.ooff = a.out_offsets ? __ldg(a.out_offsets + lo) : it.qoff;
+    }
     it.t0 = qb * 2 * TQ;
     it.ta_last = min(it.t0 + TQ, E) - 1;
     it.live_b = it.t0 + TQ < E;
@@ -297,8 +322,13 @@ __device__ __forceinline__ Item load_item(const ExtendArgs &a, const int32_t *s_
 
 }  // namespace
 
+template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
-    extend_kernel(const ExtendArgs a, const float scale_log2, const int log2g, const int slot) {
+    extend_kernel(const ExtendArgs a, const float scale_log2, const int G, const int slot) {
+    using L = Smem<D>;
+    constexpr int TILE_BYTES = L::TILE_BYTES;
+    constexpr int OFF_Q = L::OFF_Q, OFF_KV = L::OFF_KV, OFF_BAR = L::OFF_BAR;
+    constexpr int OFF_TMEM_SLOT = L::OFF_TMEM_SLOT, OFF_RING = L::OFF_RING, OFF_PREFIX = L::OFF_PREFIX;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -318,10 +348,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     int32_t *s_prefix = reinterpret_cast<int32_t *>(base + OFF_PREFIX);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int B = a.batch, Hkv = a.num_kv_heads, Hq = a.num_q_heads, W = a.pt_width;
-    const int G = 1 << log2g;
-    const int TQ = ROWS >> log2g;  // new tokens per query tile
-    const int TQ2 = 2 * TQ;        // new tokens per work item
+    const int B = a.batch, Hkv = a.num_kv_heads, Hq = a.num_q_heads;
+    const int TQ = ROWS / G;        // new tokens per query tile
+    const int TQ2 = 2 * TQ;         // new tokens per work item
+    const int live_rows = TQ * G;   // MMA rows that hold a (token, head) pair
 
     pdl_wait();
     pdl_launch_dependents();
@@ -353,9 +383,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int r = b0 + lane;
             int v = 0;
             if (r < B) {
-                const int c = min(max(__ldg(a.cached_lens + r), 0), W);
-                const int e = a.prefix_only ? max(__ldg(a.extend_lens + r), 0)
-                                            : min(max(__ldg(a.extend_lens + r), 0), W - c);
+                int c, e;
+                req_lens(a, r, c, e);
                 v = ((e + TQ2 - 1) / TQ2) * Hkv;
                 if (a.prefix_only && c == 0) v = 0;  // nothing to attend to: no items
             }
@@ -380,6 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const __nv_bfloat16 *Vl = static_cast<const __nv_bfloat16 *>(a.v_layer);
     const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.q);
     const uint32_t idesc_qk = idesc_bf16_f32(ROWS, ROWS, false);
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     const uint32_t idesc_pv = idesc_bf16_f32(ROWS, D, true);
 
     // Schedule: the CTA's first item is blockIdx.x, later ones come from a
@@ -395,20 +425,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     // The roles run through the items without a CTA-wide barrier in between;
     // each keeps its own running counts of KV tiles and of tiles per query
     // tile.
-    SchedSlot *sched = &g_sched[slot];
+    SchedSlot *sched = a.sched ? reinterpret_cast<SchedSlot *>(a.sched) : &g_sched[slot];
     if (warp >= PRODUCER_WARP0 && warp < PRODUCER_WARP0 + PRODUCER_WARPS) {
         // ---------------- producer: Q_A, Q_B per item, then K/V tiles ----------------
-        // Q tiles: thread pt copies 16-byte chunk cc of rows tb*32 .. tb*32+31
-        // (16 threads cover one 256-byte row).  K/V tiles: lane (rl = lane / 4,
-        // qq = lane % 4) of producer warp pw copies chunks qq, qq+4, qq+8,
-        // qq+12 of tokens 16m + 8pw + rl (m = 0..7), so one page-table entry
-        // and one address serve 8 copies; each warp instruction still writes
-        // 8 rows x 64 bytes that fall on distinct banks (4 wavefronts for 512
-        // bytes).  An item's Q goes out with its first K/V tile, once the MMA
+        // Q tiles: thread pt copies 16-byte chunk cc of rows tb*RPT ..
+        // tb*RPT+RPT-1 (d/8 threads cover one row of 2d bytes).  K/V tiles:
+        // lane (rl = lane / 4, qq = lane % 4) of producer warp pw copies chunks
+        // qq, qq+4, ... (d/32 of them) of tokens 16m + 8pw + rl (m = 0..7), so
+        // one page-table entry and one address serve 2d/32 copies; each warp
+        // instruction still writes 8 rows x 64 bytes that fall on distinct
+        // banks (4 wavefronts for 512 bytes).  An item's Q goes out with its first K/V tile, once the MMA
         // warp has released the Q buffers (the previous item's last S is done).
-        constexpr int RPT = ROWS * 16 / PRODUCER_THREADS;  // rows per thread: 32
+        constexpr int CPR = D / 8;                          // 16-byte chunks per row
+        constexpr int RPT = ROWS * CPR / PRODUCER_THREADS;  // Q rows per thread: 32 (d 128), 16 (d 64)
+        constexpr int CI = D / 32;                          // K/V chunks a lane copies per token row
         const int pt = threadIdx.x - PRODUCER_WARP0 * 32;
-        const int cc = pt & 15, tb = pt >> 4;
+        const int cc = pt % CPR, tb = pt / CPR;
+        const int tok0 = (tb * RPT) / G, hh0 = (tb * RPT) - tok0 * G;  // (token, head) of row tb*RPT
         uint32_t kv_iter = 0, n_items = 0;
         int item = blockIdx.x;  // this CTA's n-th item (thread 0's copy)
         for (;; ++n_items) {
@@ -447,17 +480,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (j == 0) {
                     if (n_items > 0) wait(q_empty, (n_items - 1) & 1);
 #pragma unroll
-                    for (int x = 0; x < 2; ++x)
+                    for (int x = 0; x < 2; ++x) {
+                        int tk = tok0, hd = hh0;  // (token, head) of row i, stepped along
 #pragma unroll 4
                         for (int k = 0; k < RPT; ++k) {
                             const int i = tb * RPT + k;
-                            const int t = cur.t0 + x * TQ + (i >> log2g);
-                            const bool live = t <= (x ? cur.tb_last : cur.ta_last) && (x == 0 || cur.live_b);
+                            const int t = cur.t0 + x * TQ + tk;
+                            const bool live = i < live_rows && t <= (x ? cur.tb_last : cur.ta_last) &&
+                                              (x == 0 || cur.live_b);
                             const __nv_bfloat16 *src =
-                                live ? Q + ((int64_t)(cur.qoff + t) * Hq + cur.g * G + (i & (G - 1))) * D + cc * 8
-                                     : Q;
+                                live ? Q + ((int64_t)(cur.qoff + t) * Hq + cur.g * G + hd) * D + cc * 8 : Q;
                             cp_async_16(sQ + x * TILE_BYTES + sw128(i, cc), src, live ? 16 : 0);
+                            if (++hd == G) {
+                                hd = 0;
+                                ++tk;
+                            }
                         }
+                    }
                 }
                 const uint32_t sK = sKV + st * 2 * TILE_BYTES, sV = sK + TILE_BYTES;
 #pragma unroll
@@ -467,7 +506,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int bytes = row >= 0 ? 16 : 0;
                     const uint32_t ob = (uint32_t)((2 * mm + pw) * 1024 + rl * 128);
 #pragma unroll
-                    for (int ci = 0; ci < 4; ++ci) {
+                    for (int ci = 0; ci < CI; ++ci) {
                         const uint32_t o = ob + (uint32_t)((ci >> 1) * HALF) + ((ci & 1) ? xo1 : xo0);
                         cp_async_16(sK + o, Kl + e + 32 * ci, bytes);
                         cp_async_16(sV + o, Vl + e + 32 * ci, bytes);
@@ -606,8 +645,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int nkv_x = x ? cur.nkv_b : cur.nkv_a;
             if (nkv_x > 0) {
                 const int t_last = x ? cur.tb_last : cur.ta_last;
-                const int tt = cur.t0 + x * TQ + (i >> log2g);
-                const bool live = tt <= t_last;
+                const int tt = cur.t0 + x * TQ + i / G;
+                const bool live = i < live_rows && tt <= t_last;
                 const int t = min(tt, t_last);
                 const int lim = a.prefix_only ? cur.C - 1 : cur.C + t;  // last visible position
                 float m = -INFINITY;            // running max of scaled scores (base 2)
@@ -681,7 +720,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             l2 = f2(la * alpha, lb * alpha);
                             m = m_new;
 #pragma unroll 1
-                            for (int q4 = 0; q4 < 4; ++q4) {
+                            for (int q4 = 0; q4 < D / 32; ++q4) {
                                 uint32_t o[32];
                                 tmem_ld32(ocol + 32 * q4, o);
                                 tmem_wait_ld();
@@ -717,13 +756,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // epilogue: O / l -> bf16
                 wait(pv_done(x), (cnt + nkv_x - 1) & 1);
                 tc_fence_after();
-                const float inv = 1.f / l;
-                const int64_t orow = (int64_t)(cur.ooff + t) * Hq + cur.g * G + (i & (G - 1));
+                float inv = 1.f / l;
+                const int64_t orow = (int64_t)(cur.ooff + t) * Hq + cur.g * G + (i % G);
+                // with a partial over other positions to fold in: out = (w_s o/l + w_p o_p) / (w_s + w_p),
+                // w = 2^(lse - max) in base 2 (this row's lse is m + log2 l)
+                float cp = 0.f;
+                const float *mrow = nullptr;
+                if (a.merge_o && live) {
+                    const float ls = m + log2f(l), lp = a.merge_lse[orow] * LOG2E;
+                    const float mx = fmaxf(ls, lp);
+                    const float ws = ex2(ls - mx), wp = ex2(lp - mx);
+                    const float it = 1.f / (ws + wp);
+                    inv *= ws * it;
+                    cp = wp * it;
+                    mrow = a.merge_o + orow * D;
+                }
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + orow * D;
                 if (a.out_f32 && live)  // natural-log LSE of the scaled scores
                     a.lse_out[orow] = (m + log2f(l)) * 0.6931471805599453f;
 #pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q4 = 0; q4 < D / 32; ++q4) {
                     uint32_t o[32];
                     tmem_ld32(ocol + 32 * q4, o);
                     tmem_wait_ld();
@@ -735,6 +787,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 *reinterpret_cast<float4 *>(fd + c) =
                                     make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
                                                 __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                        }
+                    } else if (mrow) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            const float4 p0 = *reinterpret_cast<const float4 *>(mrow + 32 * q4 + c);
+                            const float4 p1 = *reinterpret_cast<const float4 *>(mrow + 32 * q4 + c + 4);
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[c + 0]) * inv + cp * p0.x,
+                                              __uint_as_float(o[c + 1]) * inv + cp * p0.y);
+                            v.y = pack_bf16x2(__uint_as_float(o[c + 2]) * inv + cp * p0.z,
+                                              __uint_as_float(o[c + 3]) * inv + cp * p0.w);
+                            v.z = pack_bf16x2(__uint_as_float(o[c + 4]) * inv + cp * p1.x,
+                                              __uint_as_float(o[c + 5]) * inv + cp * p1.y);
+                            v.w = pack_bf16x2(__uint_as_float(o[c + 6]) * inv + cp * p1.z,
+                                              __uint_as_float(o[c + 7]) * inv + cp * p1.w);
+                            *reinterpret_cast<uint4 *>(dst + 32 * q4 + c) = v;
                         }
                     } else if (live) {
 #pragma unroll
@@ -780,40 +848,58 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
-    if (a.batch == 0 || a.total_q_tokens == 0) return cudaSuccess;
-    const int G = a.num_q_heads / a.num_kv_heads;
-    int log2g = 0;
-    while ((1 << log2g) < G) ++log2g;
-    const int TQ2 = 2 * (ROWS >> log2g);
-    const size_t smem = (size_t)OFF_PREFIX + (size_t)(a.batch + 1) * 4 + 1024;
+namespace {
+
+// Raise the kernel's dynamic shared-memory limit once per device.
+template <int D>
+cudaError_t configure_extend() {
     static std::mutex mu;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        if (dev >= 0 && dev < 64 && !configured[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 OFF_PREFIX + 4097 * 4 + 1024);
-            if (e != cudaSuccess) {
-                cudaGetLastError();
-                return e;
-            }
-            configured[dev] = true;
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(extend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Smem<D>::OFF_PREFIX + 4097 * 4 + 1024);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return e;
         }
+        configured[dev] = true;
     }
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_extend_d(const ExtendArgs &a, cudaStream_t s, int grid) {
+    if (cudaError_t e = configure_extend<D>()) return e;
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const size_t smem = (size_t)Smem<D>::OFF_PREFIX + (size_t)(a.batch + 1) * 4 + 1024;
+    // without a caller counter, a library ticket-counter slot per call, so
+    // calls running at the same time on different streams do not share one
+    static std::atomic<unsigned> next_slot{0};
+    const int slot = a.sched ? 0 : (int)(next_slot.fetch_add(1u) % SCHED_SLOTS);
+    return launch_pdl(extend_kernel<D>, dim3((unsigned)grid), dim3(THREADS), smem, s, a,
+                      a.sm_scale * LOG2E, G, slot);
+}
+
+}  // namespace
+
+int extend_grid(const ExtendArgs &a) {
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const int TQ2 = 2 * (ROWS / G);
     // upper bound on work items: every request can add one partial block
     const int64_t items = ((int64_t)a.total_q_tokens / TQ2 + a.batch) * a.num_kv_heads;
     int64_t grid = device_sm_count();
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
-    // a ticket counter slot per call, so calls running at the same time on
-    // different streams do not share one
-    static std::atomic<unsigned> next_slot{0};
-    const int slot = (int)(next_slot.fetch_add(1u) % SCHED_SLOTS);
-    return launch_pdl(extend_kernel, dim3((unsigned)grid), dim3(THREADS), smem, s, a,
-                      a.sm_scale * LOG2E, log2g, slot);
+    return (int)grid;
+}
+
+cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s) {
+    if (a.batch == 0 || a.total_q_tokens == 0) return cudaSuccess;
+    const int grid = extend_grid(a);
+    return a.head_dim == 64 ? launch_extend_d<64>(a, s, grid) : launch_extend_d<128>(a, s, grid);
 }
 
 cudaError_t read_kernel_timeouts(unsigned int *count) {

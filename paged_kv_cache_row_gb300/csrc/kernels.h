@@ -67,6 +67,15 @@ struct DecodeArgs {
     const int32_t *out_loc;
     const void *k_new, *v_new;
     int64_t new_k_stride, new_v_stride;
+    // request r's context is seq_lens[r] - len_offset positions of its
+    // page_table row (the cascade suffix: the row pointer is already moved
+    // past the shared prefix)
+    int32_t len_offset = 0;
+    // 1: every stream, whole or split, leaves fp32 partials and LSEs in the
+    // workspace (split 0 for a whole stream) and no merge kernel runs
+    int32_t partials_only = 0;
+    // > 0: a grid for at most this many SMs (the rest of the GPU runs other work)
+    int32_t max_sms = 0;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 
@@ -86,31 +95,41 @@ struct ExtendArgs {
     float *out_f32;               // optional [T, Hq, D] fp32 normalised output
     float *lse_out;               // [T, Hq] natural-log LSE, with out_f32
     const int32_t *out_offsets;   // optional [B]: first output row of each request (else q_offsets)
+    // Prefix chunks of a shared-prefix decode (with prefix_only): request c is
+    // chunk c of the prefix_len shared positions, prefix_chunk_len long (the
+    // last may be shorter), its page-table row at page_table + c*pt_stride;
+    // each chunk reads q rows 0 .. prefix_queries-1 and writes output rows
+    // c*prefix_queries ..  The length arrays are not read.  0 = off.
+    int32_t prefix_chunk_len = 0, prefix_len = 0, prefix_queries = 0;
+    // optional work-ticket counter (2 x uint32, zero before first use, left at
+    // zero); null = one of the library's 64 slots, taken in turn
+    unsigned int *sched = nullptr;
+    // request r has cached_lens[r] - len_offset cached positions in its
+    // page-table row (the cascade suffix: the row pointer is already moved
+    // past the shared prefix)
+    int32_t len_offset = 0;
+    // optional fp32 partial result of the same output rows over other
+    // positions ([T, Hq, D] normalised rows and [T, Hq] natural-log LSEs,
+    // indexed like out): folded into the bf16 output by log-sum-exp
+    const float *merge_o = nullptr, *merge_lse = nullptr;
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t s);
+// CTAs launch_extend will use for these arguments
+int extend_grid(const ExtendArgs &a);
 
-// Shared-prefix (cascade) decode: workspace-resident pseudo-request metadata
-// for the prefix-chunk extend launch, and the suffix decode's inputs/outputs.
-struct CascadeMeta {
-    int32_t *pre_cached, *pre_extend, *pre_qoff, *pre_ooff;  // [chunks] (+1 for qoff)
-    int32_t *suf_seq;                                         // [batch]: seq_len - P
-};
+// Shared-prefix (cascade) decode: the prefix part's fp32 partials (written by
+// the extend kernel in prefix-chunk mode), the suffix decode (partials only)
+// and the merge of both.
 struct CascadeArgs {
-    CascadeMeta meta;
-    const int32_t *page_table;    // [B, W]; the first shared_len columns equal in every row
-    int64_t pt_row_stride;
-    int32_t pt_width;
     const int32_t *seq_lens;      // [B]
     int32_t batch, num_q_heads, head_dim;
-    int32_t shared_len, chunks, chunk_len;
+    int32_t shared_len, chunks;
     float *pre_o, *pre_lse;       // [chunks, B, Hq, D], [chunks, B, Hq]
-    void *suf_out;                // [B, Hq, D] bf16 suffix attention
-    float *suf_lse;               // [B, Hq]
     DecodeArgs suffix;            // the suffix decode (workspace parts filled in by the caller)
     void *out;                    // [B, Hq, D] bf16
 };
-// base: the extend arguments shared with the prefix launch (q, pool layer, heads, scale)
-cudaError_t launch_cascade(const CascadeArgs &c, const ExtendArgs &base, cudaStream_t s);
+// prefix: the extend launch over the prefix chunks (prefix-chunk mode)
+cudaError_t launch_cascade(const CascadeArgs &c, const ExtendArgs &prefix, cudaStream_t s);
 
 struct RopeStoreArgs {
     void *k_layer, *v_layer;      // layer base of K / V in the pool

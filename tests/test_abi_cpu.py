@@ -86,22 +86,24 @@ def test_error_codes_on_host(lib):
     # page table narrower than its width
     assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 4, 16, 32, fake, 0.1, fake, fake,
                                    need, 0, None) == -3
-    # extend: head_dim 64 unsupported, group 3 unsupported
+    # extend: head_dim 96 unsupported, group 17 unsupported, unaligned work counter
     bad = p._PoolDesc.from_buffer_copy(d)
-    bad.head_dim = 64
-    bad.row_stride = 8 * 64
+    bad.head_dim = 96
+    bad.row_stride = 8 * 96
     assert lib.minisgl_extend_attn(ref(bad), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
-                                   0.1, fake, None) == -4
-    d3 = p._PoolDesc.from_buffer_copy(d)
-    d3.num_kv_heads = 2
-    d3.row_stride = 2 * 128
-    assert lib.minisgl_extend_attn(ref(d3), 0, fake, 6, fake, 2, 32, 32, fake, fake, fake, 10,
-                                   0.1, fake, None) == -4
+                                   0.1, fake, None, None) == -4
+    d17 = p._PoolDesc.from_buffer_copy(d)
+    d17.num_kv_heads = 1
+    d17.row_stride = 128
+    assert lib.minisgl_extend_attn(ref(d17), 0, fake, 17, fake, 2, 32, 32, fake, fake, fake, 10,
+                                   0.1, fake, None, None) == -4
+    assert lib.minisgl_extend_attn(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
+                                   0.1, fake, fake + 4, None) == -1
     # extend needs a positive, finite sm_scale
     assert lib.minisgl_extend_attn(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
-                                   -0.1, fake, None) == -1
+                                   -0.1, fake, None, None) == -1
     assert lib.minisgl_extend_attn(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10,
-                                   float("nan"), fake, None) == -1
+                                   float("nan"), fake, None, None) == -1
     # rope_store_kv: q stride below H_q*d, unaligned table, no table rows, NULL positions
     rs = lib.minisgl_rope_store_kv
     assert rs(ref(d), 0, fake, 16, 1024, fake, fake, 1024, 1024, fake, fake, 64, fake, 4, None) == -3
@@ -110,7 +112,7 @@ def test_error_codes_on_host(lib):
     assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, None, fake, 64, fake, 4, None) == -1
     assert rs(ref(d), 0, fake, 0, 2048, fake, fake, 1024, 1024, fake, fake, 64, fake, 4, None) == -1
     assert rs(ref(d), 0, fake, 16, 2048, fake, fake, 1024, 1024, fake, fake, 64, fake, 0, None) == 0
-    # cascade decode: shared_len outside [1, width], workspace too small, head_dim 64
+    # cascade decode: shared_len outside [1, width], workspace too small, head_dim 96
     cd = lib.minisgl_cascade_decode_attn
     big = lib.minisgl_cascade_workspace_bytes(4, 16, 8, 128)
     assert big > 0 and lib.minisgl_cascade_workspace_bytes(-1, 16, 8, 128) == 0
@@ -119,6 +121,16 @@ def test_error_codes_on_host(lib):
     assert cd(ref(d), 0, fake, 16, fake, 4, 32, 32, fake, 16, 0.1, fake, fake, 1024, None) == -6
     assert b"workspace" in lib.minisgl_last_error()
     assert cd(ref(bad), 0, fake, 16, fake, 4, 32, 32, fake, 16, 0.1, fake, fake, big, None) == -4
+    # cascade extend: shared_len outside [1, width], workspace too small, head_dim 96
+    ce = lib.minisgl_cascade_extend_attn
+    cbig = lib.minisgl_cascade_extend_workspace_bytes(10, 16, 128)
+    assert cbig == 256 + (10 * 16 * 128 * 4 + 255) // 256 * 256 + (10 * 16 * 4 + 255) // 256 * 256
+    assert ce(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10, 0, 0.1, fake, fake, cbig, None) == -1
+    assert ce(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10, 33, 0.1, fake, fake, cbig, None) == -1
+    assert ce(ref(d), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10, 8, 0.1, fake, fake, cbig - 1,
+              None) == -6
+    assert ce(ref(bad), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10, 8, 0.1, fake, fake, cbig,
+              None) == -4
     # empty work is a no-op that touches nothing
     assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 1024, 1024, fake, 0, None) == 0
     assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 0, 32, 32, fake, 0.1, fake, fake,

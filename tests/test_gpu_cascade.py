@@ -47,7 +47,7 @@ def run_cascade(case, shared_len, seq_override=None, pagefirst=False):
     torch.cuda.synchronize()
     orc = oracle.get()
     orc.store_kv(hk, hv, k_new[0].cpu(), v_new[0].cpu(), case.out_loc)
-    ref, _ = orc.decode(q[0].cpu(), hk, hv, case.page_table, seq, case.sm_scale)
+    ref, _ = gu.parallel_oracle_decode(hk, hv, q[0], case.page_table, seq, case.sm_scale)
     gu.check_attn(out, ref, f"{case.name} cascade")
     gu.check_attn(plain, ref, f"{case.name} plain decode")
     assert mk.minisgl_debug_timeout_count() == 0, "a tensor-core kernel wait ran out"
@@ -72,6 +72,60 @@ def test_cascade_decode_small(Hq, Hkv, B, P, lo, hi):
                                                     prefix_len=P, suffix_lo=lo, suffix_hi=hi,
                                                     seed=B * 31 + P)
     run_cascade(case, P)
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(6, 2, 128), (10, 2, 64), (12, 2, 64), (14, 2, 128), (8, 8, 64)])
+def test_cascade_decode_head_dims_and_odd_groups(Hq, Hkv, d):
+    """head_dim 64 and group sizes that do not divide the 128-row tile."""
+    case = workloads.make_shared_prefix_decode_case(f"cascade-g{Hq // Hkv}-d{d}", num_q_heads=Hq,
+                                                    num_kv_heads=Hkv, head_dim=d, batch=37,
+                                                    prefix_len=700, suffix_lo=0, suffix_hi=300,
+                                                    seed=Hq * 7 + d)
+    run_cascade(case, 700)
+
+
+def test_cascade_decode_prefix_fills_the_gpu():
+    """A batch whose prefix part keeps every SM busy (64 query heads, 200
+    requests, 4096 shared positions): the two parts run one after the other
+    on the caller's stream instead of side by side."""
+    case = workloads.make_shared_prefix_decode_case("cascade-wide", num_q_heads=64, num_kv_heads=8,
+                                                    head_dim=128, batch=200, prefix_len=4096,
+                                                    suffix_lo=0, suffix_hi=100, seed=97)
+    run_cascade(case, 4096)
+
+
+def test_cascade_decode_two_calls_in_a_row_on_side_streams():
+    """Consecutive cascade calls on two caller streams share the library's
+    second stream; both results stay exact."""
+    c1 = workloads.decode_shared_prefix_qwen3(prefix_len=1024)
+    c2 = workloads.make_shared_prefix_decode_case("cascade-second", num_q_heads=16, num_kv_heads=8,
+                                                  head_dim=128, batch=48, prefix_len=2000,
+                                                  suffix_lo=0, suffix_hi=400, seed=98)
+    orc = oracle.get()
+    runs = []
+    for case in (c1, c2):
+        pool_t, k_new, v_new, q = workloads.make_decode_values(case, DEV)
+        hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+        pool = mk.KVPool(pool_t)
+        pt, sl = case.page_table.to(DEV), case.seq_lens.to(DEV)
+        mk.minisgl_store_kv(pool, 0, k_new[0], v_new[0], case.out_loc.to(DEV))
+        orc.store_kv(hk, hv, k_new[0].cpu(), v_new[0].cpu(), case.out_loc)
+        ws = torch.zeros(mk.minisgl_cascade_workspace_bytes(case.batch, case.num_q_heads,
+                                                            case.num_kv_heads, case.head_dim),
+                         dtype=torch.uint8, device=DEV)
+        runs.append((case, pool, q[0], pt, sl, torch.empty_like(q[0]), ws, (hk, hv)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (case, pool, q, pt, sl, out, ws, _), st in zip(runs, streams):
+            with torch.cuda.stream(st):
+                mk.minisgl_cascade_decode_attn(pool, 0, q, pt, sl, case.shared_len, case.sm_scale,
+                                               out=out, workspace=ws)
+    torch.cuda.synchronize()
+    for case, pool, q, pt, sl, out, ws, (hk, hv) in runs:
+        ref, _ = gu.parallel_oracle_decode(hk, hv, q, case.page_table, case.seq_lens, case.sm_scale)
+        gu.check_attn(out, ref, f"{case.name} on a side stream")
+    assert mk.minisgl_debug_timeout_count() == 0
 
 
 def test_cascade_decode_empty_suffixes():

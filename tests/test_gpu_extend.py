@@ -48,16 +48,19 @@ def run_extend_case(case, check=True):
     return outs
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
-def test_extend_group_sizes(G):
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16])
+def test_extend_head_dims_and_group_sizes(G, d):
+    """Every group size 1..8 (and 12, 16) at head_dim 64 and 128.  Groups that
+    do not divide 128 leave dead MMA rows past floor(128/G)*G in each tile."""
     Hkv = 2
-    case = workloads.make_extend_case(f"g{G}", num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128,
+    case = workloads.make_extend_case(f"g{G}-d{d}", num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=d,
                                       num_reqs=3, prefix_len=70, ext_lo=1, ext_hi=260, budget=4096,
-                                      seed=300 + G)
+                                      seed=300 + G + d)
     run_extend_case(case)
 
 
-def _manual_case(cached, ext, Hq=8, Hkv=2, seed=0):
+def _manual_case(cached, ext, Hq=8, Hkv=2, seed=0, d=128):
     """Requests with given cached / extend lengths, private rows, one batch."""
     g = torch.Generator().manual_seed(seed)
     lens = [c + e for c, e in zip(cached, ext)]
@@ -73,9 +76,9 @@ def _manual_case(cached, ext, Hq=8, Hkv=2, seed=0):
         off += n
     qo = torch.zeros(len(lens) + 1, dtype=torch.int32)
     qo[1:] = torch.cumsum(torch.tensor(ext, dtype=torch.int32), 0)
-    case = workloads.ExtendCase(name="manual", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+    case = workloads.ExtendCase(name="manual", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
                                 num_rows=R, prefix_rows=perm[:0], extend_lens=list(ext),
-                                sm_scale=1 / 128 ** 0.5, value_std=0.5, seed=seed)
+                                sm_scale=1 / d ** 0.5, value_std=0.5, seed=seed)
     case.batches.append(workloads.ExtendBatch(
         req_ids=list(range(len(lens))), cached_lens=torch.tensor(cached, dtype=torch.int32),
         extend_lens=torch.tensor(ext, dtype=torch.int32), q_offsets=qo, page_table=pt,
@@ -83,12 +86,47 @@ def _manual_case(cached, ext, Hq=8, Hkv=2, seed=0):
     return case
 
 
-def test_extend_edge_lengths():
-    """No prefix, one-token extends, extends ending exactly on tile edges,
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (6, 2, 64), (14, 2, 128)])
+def test_extend_edge_lengths(Hq, Hkv, d):
+    """No prefix, one-token extends, extends ending exactly on tile edges and
+    on query-tile edges (42 tokens per tile at group 3, 18 at group 7),
     prefixes ending on tile edges, and an empty extend in the middle."""
-    cached = [0, 0, 128, 5, 127, 300, 0, 256]
-    ext = [1, 128, 1, 0, 129, 33, 257, 64]
-    run_extend_case(_manual_case(cached, ext, seed=41))
+    cached = [0, 0, 128, 5, 127, 300, 0, 256, 0, 10]
+    ext = [1, 128, 1, 0, 129, 33, 257, 64, 42, 85]
+    run_extend_case(_manual_case(cached, ext, Hq=Hq, Hkv=Hkv, seed=41, d=d))
+
+
+def test_extend_caller_counters_on_two_streams():
+    """Two extend calls at a time on two unordered streams, each with its own
+    work counter, three rounds: both match the oracle and both counters are
+    back at zero afterwards."""
+    cases = [_manual_case([300, 0, 900], [700, 513, 260], Hq=32, Hkv=8, seed=61),
+             _manual_case([0, 1500], [1000, 300], Hq=32, Hkv=8, seed=62)]
+    orc = oracle.get()
+    runs = []
+    for case in cases:
+        pool_t, per_batch = workloads.make_extend_values(case, DEV)
+        hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+        pool = mk.KVPool(pool_t)
+        b = case.batches[0]
+        k, v, q = per_batch[0]
+        mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+        orc.store_kv(hk, hv, k.cpu(), v.cpu(), b.out_loc)
+        args = (b.page_table.to(DEV), b.cached_lens.to(DEV), b.extend_lens.to(DEV), b.q_offsets.to(DEV))
+        runs.append((case, pool, q, args, torch.empty_like(q), mk.extend_work_counter(), (hk, hv)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (case, pool, q, args, out, ctr, _), st in zip(runs, streams):
+            with torch.cuda.stream(st):
+                mk.minisgl_extend_attn(pool, 0, q, *args, case.sm_scale, out=out, work_counter=ctr)
+    torch.cuda.synchronize()
+    for case, pool, q, args, out, ctr, (hk, hv) in runs:
+        b = case.batches[0]
+        ref = orc.extend(q.cpu(), hk, hv, b.page_table, b.cached_lens, b.extend_lens, case.sm_scale)
+        gu.check_attn(out, ref, "extend with a caller counter")
+        assert ctr.cpu().tolist() == [0, 0], "work counter not left at zero"
+    assert mk.minisgl_debug_timeout_count() == 0
 
 
 def test_extend_mixed_chunk_and_decode_batch():
@@ -249,4 +287,29 @@ def test_extend_and_decode_on_pagefirst_pool():
     orc.store_kv(dk, dv, k_new[0].cpu(), v_new[0].cpu(), dcase.out_loc)
     ref, _ = orc.decode(q[0].cpu(), dk, dv, dcase.page_table, dcase.seq_lens, dcase.sm_scale)
     gu.check_attn(out, ref, "pagefirst decode")
+    assert mk.minisgl_debug_timeout_count() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,P", [(8, 2, 128, 300), (32, 8, 128, 1000), (6, 2, 64, 129),
+                                         (14, 2, 64, 64), (16, 16, 128, 1)])
+def test_cascade_extend_matches_oracle(Hq, Hkv, d, P):
+    """Shared-prefix extend over chunked batches: a request cut by the budget
+    continues with cached_len > P; prefixes shorter than, equal to and longer
+    than one tile, one shared position, head_dim 64, odd groups."""
+    case = workloads.make_extend_case(f"cascade-ext-g{Hq // Hkv}-d{d}-p{P}", num_q_heads=Hq,
+                                      num_kv_heads=Hkv, head_dim=d, num_reqs=5, prefix_len=P,
+                                      ext_lo=1, ext_hi=400, budget=700, seed=500 + P + d)
+    assert len(case.batches) >= 2
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+    pool = mk.KVPool(pool_t)
+    orc = oracle.get()
+    for bi, (b, (k, v, q)) in enumerate(zip(case.batches, per_batch)):
+        mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+        o = mk.minisgl_cascade_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                                           b.extend_lens.to(DEV), b.q_offsets.to(DEV), P, case.sm_scale)
+        torch.cuda.synchronize()
+        orc.store_kv(hk, hv, k.cpu(), v.cpu(), b.out_loc)
+        ref = orc.extend(q.cpu(), hk, hv, b.page_table, b.cached_lens, b.extend_lens, case.sm_scale)
+        gu.check_attn(o, ref, f"{case.name} batch {bi}")
     assert mk.minisgl_debug_timeout_count() == 0

@@ -91,7 +91,8 @@ def test_full_long_page64_decode():
 
 
 def test_full_radix_shared_extend():
-    """Every new token of every chunked-prefill batch against the oracle."""
+    """Every new token of every chunked-prefill batch against the oracle, for
+    the extend call and for the shared-prefix (cascade) extend call."""
     case = workloads.extend_radix_shared()
     assert 2 <= len(case.batches) <= 5
     pool_t, per_batch = workloads.make_extend_values(case, DEV)
@@ -111,6 +112,13 @@ def test_full_radix_shared_extend():
                                         b.q_offsets, case.sm_scale)
         stats = gu.check_attn(o, ref, f"extend batch {bi} (all {b.total_tokens} tokens)")
         print(f"extend batch {bi}: {stats}")
+        # the shared-prefix (cascade) extend of the same batch: same oracle values
+        oc = mk.minisgl_cascade_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                                            b.extend_lens.to(DEV), b.q_offsets.to(DEV),
+                                            int(case.prefix_rows.numel()), case.sm_scale)
+        torch.cuda.synchronize()
+        stats = gu.check_attn(oc, ref, f"cascade extend batch {bi} (all {b.total_tokens} tokens)")
+        print(f"cascade extend batch {bi}: {stats}")
     assert mk.minisgl_debug_timeout_count() == 0
 
 

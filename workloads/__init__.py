@@ -496,3 +496,30 @@ def mixed_chunk_decode(seed: int = 1006, num_decode: int = 64, ctx_lo: int = 512
                                     page_table=pt, out_loc=torch.cat(outs).to(torch.int32)))
     case.num_decode = num_decode  # type: ignore[attr-defined]
     return case
+
+
+# --------------------------------------------------------------------------- #
+# store_kv at scale: several disjoint extend-sized batches
+# --------------------------------------------------------------------------- #
+@dataclass
+class StoreRotation:
+    name: str
+    num_rows: int
+    num_kv_heads: int
+    head_dim: int
+    out_locs: List[torch.Tensor]  # one [tokens] int32 per batch, rows disjoint across batches
+    seed: int
+
+
+def store_rotation(seed: int = 1007, batches: int = 8, tokens: int = 8192, num_kv_heads: int = 8,
+                   head_dim: int = 128, pool_factor: float = 1.2) -> StoreRotation:
+    """`batches` store_kv batches of `tokens` new tokens each (the chunked-prefill
+    budget of the radix-shared extend workload), with disjoint random rows of
+    one pool, so that storing them one after the other touches more memory than
+    the L2 holds (8 x 67 MB at the defaults)."""
+    g = torch.Generator().manual_seed(seed)
+    live = int(math.ceil(pool_factor * batches * tokens))
+    perm = torch.randperm(live, generator=g).to(torch.int32)
+    locs = [perm[b * tokens:(b + 1) * tokens].clone() for b in range(batches)]
+    return StoreRotation(name=f"store-kv-{batches}x{tokens}-tokens", num_rows=live + 2,
+                         num_kv_heads=num_kv_heads, head_dim=head_dim, out_locs=locs, seed=seed)
