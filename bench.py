@@ -476,13 +476,29 @@ def bench_store_kv_at_scale(mk, args, dev, stream, peaks):
     reps = max(5, args.steps // 4)
     ms = ev_time(lambda: [rotation() for _ in range(reps)], 1, stream) / (reps * len(locs))
     s_b = n * (2 * 2 * Hkv * d * 2 + 4)
+    # context: a plain device copy of the same bytes (k and v of a batch into a
+    # contiguous buffer), in the same rotation, by torch
+    cdst = [torch.empty((2, n, Hkv, d), dtype=torch.bfloat16, device=dev) for _ in locs]
+
+    def copy_rotation():
+        for k, v, c in zip(ks, vs, cdst):
+            c[0].copy_(k)
+            c[1].copy_(v)
+
+    for _ in range(args.warmup):
+        copy_rotation()
+    c_ms = ev_time(lambda: [copy_rotation() for _ in range(reps)], 1, stream) / (reps * len(locs))
     res = {"workload": rot.name, "tokens": n, "algorithmic_bytes": s_b,
            "ms_per_launch": round(ms, 5), "achieved_gbs": round(s_b / (ms * 1e-3) / 1e9, 1),
            "frac_of_hbm": round(s_b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "traffic": profile_traffic("store_kv.cu", "store_kv_extend_batch.md"),
            "launches_timed": reps * len(locs),
+           "same_size_copy": {"ms": round(c_ms, 5), "gbs": round(s_b / (c_ms * 1e-3) / 1e9, 1),
+                              "what": "torch copy of the same k and v bytes into contiguous buffers, "
+                                      "same rotation (two copy kernels per batch)",
+                              "store_kv_relative": round(c_ms / ms, 4)},
            "l2": "8 batches with disjoint rows stored in turn: 536 MB per rotation, larger than L2"}
-    del pool_t, ks, vs
+    del pool_t, ks, vs, cdst
     torch.cuda.empty_cache()
     return res
 

@@ -153,6 +153,8 @@ int minisgl_store_kv(const minisgl_kv_pool *pool, int32_t layer, const void *k, 
         return fail(MINISGL_ERR_SHAPE, "store_kv: k and v must be 16-byte aligned");
     if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
         return fail(MINISGL_ERR_SHAPE, "store_kv: token strides must be >= H_kv*d and multiples of 8");
+    if ((int64_t)n_tokens * (row / 4) >= (int64_t(1) << 31))
+        return fail(MINISGL_ERR_UNSUPPORTED, "store_kv: n_tokens * H_kv * d too large for one call");
     minisgl::StoreArgs a;
     a.k_layer = const_cast<void *>(layer_ptr(pool->k_base, pool, layer));
     a.v_layer = const_cast<void *>(layer_ptr(pool->v_base, pool, layer));
@@ -347,7 +349,7 @@ namespace {
 
 constexpr int CASCADE_MAX_CHUNKS = 32;
 
-constexpr int CASCADE_SUFFIX_SPLITS = 16;
+constexpr int CASCADE_SUFFIX_SPLITS = 16;  // the merge kernel holds at most 16 suffix splits
 
 // Workspace layout of minisgl_cascade_decode_attn (each part 256-byte aligned):
 // the prefix launch's work-ticket counter (8 bytes in a 256-byte part), fp32

@@ -36,24 +36,59 @@ namespace {
 
 // one warp per (request, query head): merge the prefix chunks' fp32 partials
 // (lane c holds chunk c's LSE) and the suffix's split partials (lane s holds
-// split s's LSE; none when the request has no private positions)
+// split s's LSE; none when the request has no private positions).  Two
+// rounds of loads: first the context length, the split count and everything
+// of the prefix (LSEs and up to PF rows), which do not depend on the split
+// count; then the suffix LSEs and rows (at most SMAX).
 template <int D>
 __global__ void __launch_bounds__(256) cascade_merge_kernel(CascadeArgs a) {
     pdl_wait();
     pdl_launch_dependents();
-    constexpr int PER = D / 32;  // channels per lane
+    constexpr int PER = D / 32;  // channels per lane: 4 (d 128) or 2 (d 64)
+    static_assert(PER == 4 || PER == 2, "head_dim 64 or 128");
+    constexpr int PF = 8;        // prefix rows loaded in the first round
+    constexpr int SMAX = 16;     // suffix splits (the cascade call uses 16)
     const int lane = threadIdx.x & 31;
     const DecodeArgs &sd = a.suffix;
     const int G = a.num_q_heads / sd.num_kv_heads;
     const int64_t nvec = (int64_t)a.batch * a.num_q_heads;
+    auto load_row = [&](const float *o, float (&x)[PER]) {
+        if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(o);
+            x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2 *>(o);
+            x[0] = t.x, x[1] = t.y;
+        }
+    };
     for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < nvec;
          v += ((int64_t)gridDim.x * blockDim.x) >> 5) {
         const int r = (int)(v / a.num_q_heads), h = (int)(v - (int64_t)r * a.num_q_heads);
-        const int n_suf = min(max(__ldg(a.seq_lens + r) - a.shared_len, 0), sd.pt_width);
-        const int S = n_suf > 0 ? min(sd.split_count[(int64_t)r * sd.num_kv_heads + h / G], sd.max_splits) : 0;
-        const int64_t sbase = v * sd.max_splits;
+        // round 1
+        const int seq = __ldg(a.seq_lens + r);
+        const int cnt = sd.split_count[(int64_t)r * sd.num_kv_heads + h / G];  // stale if no suffix: unused then
         const float lp = lane < a.chunks ? a.pre_lse[(int64_t)lane * nvec + v] : -INFINITY;
+        float xp[PF][PER];
+#pragma unroll
+        for (int k = 0; k < PF; ++k) {
+            if (k < a.chunks) load_row(a.pre_o + ((int64_t)k * nvec + v) * D + lane * PER, xp[k]);
+            else
+#pragma unroll
+                for (int c = 0; c < PER; ++c) xp[k][c] = 0.f;
+        }
+        // round 2
+        const int n_suf = min(max(seq - a.shared_len, 0), sd.pt_width);
+        const int S = n_suf > 0 ? min(min(cnt, sd.max_splits), SMAX) : 0;
+        const int64_t sbase = v * sd.max_splits;
         const float ls = lane < S ? sd.ws_lse[sbase + lane] : -INFINITY;
+        float xs[SMAX][PER];
+#pragma unroll
+        for (int k = 0; k < SMAX; ++k) {
+            if (k < S) load_row(sd.ws_o + (sbase + k) * D + lane * PER, xs[k]);
+            else
+#pragma unroll
+                for (int c = 0; c < PER; ++c) xs[k][c] = 0.f;
+        }
         float top = fmaxf(lp, ls);
 #pragma unroll
         for (int o = 16; o; o >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
@@ -65,29 +100,24 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(CascadeArgs a) {
         float acc[PER];
 #pragma unroll
         for (int c = 0; c < PER; ++c) acc[c] = 0.f;
-        for (int p = 0; p < a.chunks; ++p) {
-            const float w = __shfl_sync(0xffffffffu, wp, p);
-            const float *o = a.pre_o + ((int64_t)p * nvec + v) * D + lane * PER;
 #pragma unroll
-            for (int c = 0; c < PER; c += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(o + c);
-                acc[c] += w * x.x;
-                acc[c + 1] += w * x.y;
-                acc[c + 2] += w * x.z;
-                acc[c + 3] += w * x.w;
-            }
+        for (int k = 0; k < PF; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wp, k);  // 0 past the chunks
+#pragma unroll
+            for (int c = 0; c < PER; ++c) acc[c] += w * xp[k][c];
         }
-        for (int s = 0; s < S; ++s) {
-            const float w = __shfl_sync(0xffffffffu, ws, s);
-            const float *o = sd.ws_o + (sbase + s) * D + lane * PER;
+        for (int k = PF; k < a.chunks; ++k) {  // more than PF chunks: one row at a time
+            float x[PER];
+            load_row(a.pre_o + ((int64_t)k * nvec + v) * D + lane * PER, x);
+            const float w = __shfl_sync(0xffffffffu, wp, k);
 #pragma unroll
-            for (int c = 0; c < PER; c += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(o + c);
-                acc[c] += w * x.x;
-                acc[c + 1] += w * x.y;
-                acc[c + 2] += w * x.z;
-                acc[c + 3] += w * x.w;
-            }
+            for (int c = 0; c < PER; ++c) acc[c] += w * x[c];
+        }
+#pragma unroll
+        for (int k = 0; k < SMAX; ++k) {
+            const float w = __shfl_sync(0xffffffffu, ws, k);  // 0 past S
+#pragma unroll
+            for (int c = 0; c < PER; ++c) acc[c] += w * xs[k][c];
         }
         const float inv = 1.f / total;
         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + v * D + lane * PER;

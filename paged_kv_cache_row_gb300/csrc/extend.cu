@@ -90,13 +90,17 @@ struct Smem {
     static constexpr int OFF_PREFIX = OFF_RING + RING * 64;
 };
 constexpr int THREADS = 384;              // 2 softmax warpgroups, 2 producer warps, idle warp, MMA warp
+constexpr int SOFTMAX_WARP0 = 0;          // warps SOFTMAX_WARP0 .. +3: tile A; +4 .. +7: tile B
 constexpr int PRODUCER_WARP0 = 8;
 constexpr int PRODUCER_THREADS = 64;
 constexpr int PRODUCER_WARPS = 2;
 // The MMA issuer is warp 11: warps are spread over the four schedulers by
 // warp index mod 4, and scheduler 3 carries only softmax warps 3 and 7
 // besides it (warp 10, on scheduler 2 with softmax warps 2 and 6, idles).
+// A softmax warp may only touch the tensor-memory lane quarter warp % 4, so
+// SOFTMAX_WARP0 must be a multiple of 4.
 constexpr int MMA_WARP = 11;
+static_assert(SOFTMAX_WARP0 % 4 == 0, "softmax warpgroups start on a lane-quarter boundary");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.f;
@@ -626,13 +630,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 8) {
+    } else if (warp >= SOFTMAX_WARP0 && warp < SOFTMAX_WARP0 + 8) {
         // ---------------- softmax / epilogue: thread i owns row i of tile x ----------------
         // O_X is read out before this warpgroup publishes the next item's
         // first P_X, and the MMA that overwrites O_X (that item's first PV_X)
         // waits for that P_X.
-        const int x = warp >> 2;
-        const int i = threadIdx.x - x * 128;
+        const int x = (warp - SOFTMAX_WARP0) >> 2;
+        const int i = threadIdx.x - SOFTMAX_WARP0 * 32 - x * 128;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t scol = lane_base + col_s(x), ocol = lane_base + col_o(x);
         const uint64_t scale2 = f2(scale_log2, scale_log2);
@@ -888,8 +892,11 @@ cudaError_t launch_extend_d(const ExtendArgs &a, cudaStream_t s, int grid) {
 int extend_grid(const ExtendArgs &a) {
     const int G = a.num_q_heads / a.num_kv_heads;
     const int TQ2 = 2 * (ROWS / G);
-    // upper bound on work items: every request can add one partial block
-    const int64_t items = ((int64_t)a.total_q_tokens / TQ2 + a.batch) * a.num_kv_heads;
+    // work items: exact for prefix chunks (every chunk has all the queries),
+    // else an upper bound (every request can add one partial block)
+    const int64_t items = a.prefix_chunk_len > 0
+                              ? (int64_t)a.batch * ((a.prefix_queries + TQ2 - 1) / TQ2) * a.num_kv_heads
+                              : ((int64_t)a.total_q_tokens / TQ2 + a.batch) * a.num_kv_heads;
     int64_t grid = device_sm_count();
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;

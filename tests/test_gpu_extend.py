@@ -298,7 +298,7 @@ def test_cascade_extend_matches_oracle(Hq, Hkv, d, P):
     than one tile, one shared position, head_dim 64, odd groups."""
     case = workloads.make_extend_case(f"cascade-ext-g{Hq // Hkv}-d{d}-p{P}", num_q_heads=Hq,
                                       num_kv_heads=Hkv, head_dim=d, num_reqs=5, prefix_len=P,
-                                      ext_lo=1, ext_hi=400, budget=700, seed=500 + P + d)
+                                      ext_lo=1, ext_hi=400, budget=300, seed=500 + P + d)
     assert len(case.batches) >= 2
     pool_t, per_batch = workloads.make_extend_values(case, DEV)
     hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
