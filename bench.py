@@ -661,10 +661,11 @@ def bench_mixed(mk, args, dev, stream, flush):
 
 def bench_cascade(mk, args, dev, stream, peaks, flush):
     """Shared-prefix (cascade) decode against plain decode on radix-shared
-    batches with a 4096- and a 1024-token prefix."""
+    batches with a 4096-, a 1024- and a 256-token prefix."""
     casc = []
     for sc in (workloads.decode_shared_prefix_qwen3(),
-               workloads.decode_shared_prefix_qwen3(prefix_len=1024)):
+               workloads.decode_shared_prefix_qwen3(prefix_len=1024),
+               workloads.decode_shared_prefix_qwen3(prefix_len=256)):
         spool_t, sk, sv, sq = workloads.make_decode_values(sc, dev)
         spool = mk.KVPool(spool_t)
         spt, ssl, sloc = sc.page_table.to(dev), sc.seq_lens.to(dev), sc.out_loc.to(dev)

@@ -29,7 +29,7 @@ __all__ = [
     "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv", "minisgl_cascade_decode_attn",
     "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn", "minisgl_check_indices",
     "minisgl_debug_set_pdl", "extend_work_counter", "minisgl_cascade_extend_attn",
-    "minisgl_cascade_extend_workspace_bytes",
+    "minisgl_cascade_extend_workspace_bytes", "minisgl_check_shared_prefix",
 ]
 
 EXPORTED_SYMBOLS = [
@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = [
     "minisgl_debug_timeout_count", "minisgl_decode_attn_noalloc", "minisgl_rope_store_kv",
     "minisgl_cascade_decode_attn", "minisgl_cascade_workspace_bytes", "minisgl_store_decode_attn",
     "minisgl_check_indices", "minisgl_debug_set_pdl", "minisgl_cascade_extend_attn",
-    "minisgl_cascade_extend_workspace_bytes",
+    "minisgl_cascade_extend_workspace_bytes", "minisgl_check_shared_prefix",
 ]
 
 MINISGL_BF16 = 1
@@ -107,6 +107,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.minisgl_cascade_extend_attn.argtypes = [P, i32, vp, i32, vp, i32, i64, i32, vp, vp, vp, i32, i32,
                                                 f32, vp, vp, sz, vp]
     lib.minisgl_cascade_extend_attn.restype = ctypes.c_int
+    lib.minisgl_check_shared_prefix.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp]
+    lib.minisgl_check_shared_prefix.restype = ctypes.c_int
     lib.minisgl_debug_set_pdl.argtypes = [ctypes.c_int]
     lib.minisgl_debug_set_pdl.restype = ctypes.c_int
     _lib = lib
@@ -514,3 +516,27 @@ def minisgl_cascade_extend_attn(pool: KVPool, layer: int, q: torch.Tensor, page_
                                            float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
                                            _stream(stream)), "cascade_extend_attn")
     return out
+
+
+def minisgl_check_shared_prefix(page_table: torch.Tensor, lens: torch.Tensor, shared_len: int,
+                                counts: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Count, on the device, the shared-prefix page-table entries that differ
+    from the first request's and the requests shorter than shared_len:
+    returns an int32 CUDA tensor [differing entries, short requests] (read it
+    after the stream).  lens: seq_lens for decode, cached_lens for extend."""
+    lib = load_library()
+    _need(page_table, "page_table", torch.int32)
+    _need(lens, "lens", torch.int32)
+    if page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise MinisglError("page_table must be [B, W] with unit column stride")
+    if lens.numel() != page_table.shape[0] or not lens.is_contiguous():
+        raise MinisglError("lens must be a contiguous [B] tensor")
+    if counts is None:
+        counts = torch.empty(2, dtype=torch.int32, device=page_table.device)
+    _need(counts, "counts", torch.int32)
+    if counts.numel() < 2:
+        raise MinisglError("counts needs 2 elements")
+    _check(lib.minisgl_check_shared_prefix(_ptr(page_table), page_table.shape[0], page_table.stride(0),
+                                           page_table.shape[1], int(shared_len), _ptr(lens), _ptr(counts),
+                                           _stream(stream)), "check_shared_prefix")
+    return counts

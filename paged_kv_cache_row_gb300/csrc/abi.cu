@@ -653,4 +653,23 @@ int minisgl_check_indices(const int32_t *page_table, int32_t batch, int64_t pt_r
                        "check_indices");
 }
 
+int minisgl_check_shared_prefix(const int32_t *page_table, int32_t batch, int64_t pt_row_stride,
+                                int32_t pt_width, int32_t shared_len, const int32_t *lens,
+                                uint32_t *counts, void *stream) {
+    g_err.clear();
+    NvtxRange nvtx_range("minisgl_check_shared_prefix");
+    if (!counts) return fail(MINISGL_ERR_ARG, "check_shared_prefix: NULL counts");
+    if (batch < 0 || pt_width < 0)
+        return fail(MINISGL_ERR_ARG, "check_shared_prefix: negative batch or pt_width");
+    if (shared_len < 1 || shared_len > pt_width)
+        return fail(MINISGL_ERR_ARG, "check_shared_prefix: shared_len %d outside [1, pt_width]", shared_len);
+    if (batch > 0 && (!page_table || !lens))
+        return fail(MINISGL_ERR_ARG, "check_shared_prefix: NULL page_table or lens");
+    if (batch > 0 && pt_row_stride < pt_width)
+        return fail(MINISGL_ERR_SHAPE, "check_shared_prefix: need pt_width <= pt_row_stride");
+    return cuda_status(minisgl::launch_check_shared_prefix(page_table, batch, pt_row_stride, shared_len, lens,
+                                                           counts, static_cast<cudaStream_t>(stream)),
+                       "check_shared_prefix");
+}
+
 }  // extern "C"

@@ -59,4 +59,46 @@ cudaError_t launch_check_indices(const CheckArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The shared-prefix (cascade) calls trust their caller that the first
+// shared_len page-table entries are the same rows in every request and that
+// every request reads at least shared_len positions (mini-sglang-learn,
+// radix-cache chapter: requests matching a cached prefix point at its rows).
+// This kernel counts the entries that break the first condition
+// (page_table[r, j] != page_table[0, j], j < shared_len) and the requests
+// that break the second (lens[r] < shared_len).
+__global__ void __launch_bounds__(256) check_shared_prefix_kernel(const int32_t *page_table, int batch,
+                                                                  int64_t pt_stride, int shared_len,
+                                                                  const int32_t *lens, uint32_t *counts) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+    unsigned diff = 0, shorter = 0;
+    const int64_t cells = (int64_t)batch * shared_len;
+    for (int64_t k = tid; k < cells; k += nth) {
+        const int r = (int)(k / shared_len), j = (int)(k - (int64_t)r * shared_len);
+        if (r > 0) diff += __ldg(page_table + (int64_t)r * pt_stride + j) != __ldg(page_table + j) ? 1u : 0u;
+    }
+    for (int64_t k = tid; k < batch; k += nth) shorter += __ldg(lens + k) < shared_len ? 1u : 0u;
+    diff = __reduce_add_sync(0xffffffffu, diff);
+    shorter = __reduce_add_sync(0xffffffffu, shorter);
+    if ((threadIdx.x & 31) == 0) {
+        if (diff) atomicAdd(counts + 0, diff);
+        if (shorter) atomicAdd(counts + 1, shorter);
+    }
+}
+
+cudaError_t launch_check_shared_prefix(const int32_t *page_table, int32_t batch, int64_t pt_stride,
+                                       int32_t shared_len, const int32_t *lens, uint32_t *counts,
+                                       cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    const int64_t work = max((int64_t)batch * shared_len, (int64_t)batch);
+    if (work == 0) return cudaSuccess;
+    int64_t grid = (work + 255) / 256;
+    const int64_t cap = 4LL * max(device_sm_count(), 1);
+    if (grid > cap) grid = cap;
+    check_shared_prefix_kernel<<<(unsigned)grid, 256, 0, s>>>(page_table, batch, pt_stride, shared_len, lens,
+                                                              counts);
+    return cudaGetLastError();
+}
+
 }  // namespace minisgl

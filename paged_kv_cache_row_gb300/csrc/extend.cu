@@ -298,7 +298,10 @@ __device__ __forceinline__ Item load_item(const ExtendArgs &a, const int32_t *s_
     const int nqb = (s_prefix[lo + 1] - s_prefix[lo]) / a.num_kv_heads;
     const int off = item - s_prefix[lo];
     it.g = off / nqb;
-    const int qb = off - it.g * nqb;
+    // a stream's query blocks are handed out last block first: with the causal
+    // limit the last block sees the most positions, so the items drawn at the
+    // end of the launch (the tail) are the stream's shortest ones
+    const int qb = nqb - 1 - (off - it.g * nqb);
     int E;
     req_lens(a, lo, it.C, E);
     if (a.prefix_chunk_len > 0) {  // every chunk reads q rows 0.. and writes its own rows

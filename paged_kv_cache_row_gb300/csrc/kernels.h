@@ -158,6 +158,11 @@ struct CheckArgs {
     uint32_t *counts;             // [3], zeroed by the caller's stream before the launch
 };
 cudaError_t launch_check_indices(const CheckArgs &a, cudaStream_t s);
+// Count page-table entries of the shared prefix that differ from the first
+// row's and requests shorter than the prefix (counts[0], counts[1], zeroed first).
+cudaError_t launch_check_shared_prefix(const int32_t *page_table, int32_t batch, int64_t pt_stride,
+                                       int32_t shared_len, const int32_t *lens, uint32_t *counts,
+                                       cudaStream_t s);
 
 int device_sm_count();
 

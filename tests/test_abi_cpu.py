@@ -131,6 +131,13 @@ def test_error_codes_on_host(lib):
               None) == -6
     assert ce(ref(bad), 0, fake, 16, fake, 2, 32, 32, fake, fake, fake, 10, 8, 0.1, fake, fake, cbig,
               None) == -4
+    # shared-prefix check: NULL counts, shared_len outside [1, width], NULL lens
+    cs = lib.minisgl_check_shared_prefix
+    assert cs(fake, 4, 32, 32, 8, fake, None, None) == -1
+    assert cs(fake, 4, 32, 32, 0, fake, fake, None) == -1
+    assert cs(fake, 4, 32, 32, 33, fake, fake, None) == -1
+    assert cs(fake, 4, 32, 32, 8, None, fake, None) == -1
+    assert cs(fake, 4, 16, 32, 8, fake, fake, None) == -3
     # empty work is a no-op that touches nothing
     assert lib.minisgl_store_kv(ref(d), 0, fake, fake, 1024, 1024, fake, 0, None) == 0
     assert lib.minisgl_decode_attn(ref(d), 0, fake, 16, fake, 0, 32, 32, fake, 0.1, fake, fake,

@@ -73,3 +73,31 @@ def test_extend_lengths_and_empty_inputs():
     empty = torch.empty((0, 32), dtype=torch.int32, device=DEV)
     counts = mk.minisgl_check_indices(empty, torch.empty(0, dtype=torch.int32, device=DEV), 10)
     assert counts.cpu().tolist() == [0, 0, 0]
+
+
+def host_shared_prefix_counts(pt, lens, P):
+    diff = sum(int(pt[r, j] != pt[0, j]) for r in range(1, pt.shape[0]) for j in range(P))
+    short = sum(int(int(n) < P) for n in lens.tolist())
+    return [diff, short]
+
+
+def test_shared_prefix_check():
+    """minisgl_check_shared_prefix counts the prefix entries that differ from
+    the first request's and the requests shorter than the prefix: none on a
+    radix-shared batch, exactly the planted ones after corrupting it, and it
+    agrees with a host count when the declared prefix is longer than the
+    shared one."""
+    case = workloads.make_shared_prefix_decode_case("check-shared", num_q_heads=8, num_kv_heads=2,
+                                                    head_dim=128, batch=9, prefix_len=300,
+                                                    suffix_lo=0, suffix_hi=50, seed=5)
+    pt, sl = case.page_table.clone(), case.seq_lens.clone()
+    got = mk.minisgl_check_shared_prefix(pt.to(DEV), sl.to(DEV), 300)
+    assert got.cpu().tolist() == [0, 0]
+    pt[3, 17] += 1
+    pt[8, 299] = case.num_rows - 1
+    sl[2] = 299
+    got = mk.minisgl_check_shared_prefix(pt.to(DEV), sl.to(DEV), 300)
+    assert got.cpu().tolist() == [2, 1] == host_shared_prefix_counts(pt, sl, 300)
+    P = int(pt.shape[1])  # declared longer than what is shared
+    got = mk.minisgl_check_shared_prefix(pt.to(DEV), sl.to(DEV), P)
+    assert got.cpu().tolist() == host_shared_prefix_counts(pt, sl, P)
