@@ -42,9 +42,13 @@
  *   - Element type is bf16 for K, V, Q and the output (MINISGL_BF16); index
  *     tensors are int32.  Strides are in elements.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream).  No call synchronises with the host.  minisgl_store_decode_attn
- *     and minisgl_extend_attn (with minisgl_store_kv) are tested captured in
- *     a CUDA graph and replayed, with their pointers fixed.
+ *     stream).  No call synchronises with the host.  minisgl_store_decode_attn,
+ *     minisgl_extend_attn (with minisgl_store_kv; with and without a caller
+ *     work counter), minisgl_cascade_decode_attn (including its fork onto the
+ *     library's second stream and the join back) and
+ *     minisgl_cascade_extend_attn are tested captured in a CUDA graph and
+ *     replayed, with their pointers fixed; the first cascade-decode call on a
+ *     device creates that stream and its events, so make it before capture.
  *   - Return value: MINISGL_OK, or a negative MINISGL_ERR_* code with a
  *     message available from minisgl_last_error().  Argument checks happen on
  *     the host before any launch; a launch failure returns MINISGL_ERR_CUDA.
@@ -235,7 +239,8 @@ size_t minisgl_cascade_workspace_bytes(int32_t batch, int32_t num_q_heads, int32
  * minisgl_decode_attn, plus shared_len = P: the caller guarantees that the
  * first P page-table entries are the same physical rows in every row of the
  * batch and that every seq_lens[r] >= P (results are unspecified otherwise;
- * nothing is checked on the device).  The shared rows are read once per KV
+ * the call checks nothing on the device; minisgl_check_shared_prefix counts
+ * violations in a debugging run).  The shared rows are read once per KV
  * head for the whole batch instead of once per request: the P prefix
  * positions are attended by all B*G query rows of a KV head at once on the
  * tensor cores (in chunks spread over the SMs), each request's own positions
@@ -280,8 +285,9 @@ size_t minisgl_cascade_extend_workspace_bytes(int32_t total_q_tokens, int32_t nu
  * passage].  Same definition, arguments and result as minisgl_extend_attn,
  * plus shared_len = P: the caller guarantees that the first P page-table
  * entries are the same physical rows in every row of the batch and that
- * every cached_lens[r] >= P (results are unspecified otherwise; nothing is
- * checked on the device).  Two tensor-core passes: (1) every new token of the
+ * every cached_lens[r] >= P (results are unspecified otherwise; the call
+ * checks nothing on the device; minisgl_check_shared_prefix counts
+ * violations).  Two tensor-core passes: (1) every new token of the
  * batch against the P shared positions as one block, read once per KV head,
  * leaving fp32 partial rows and LSEs in the workspace; (2) each request's own
  * positions P .. C+t causally, with the partial from (1) folded in by

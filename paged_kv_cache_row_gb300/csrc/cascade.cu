@@ -144,10 +144,17 @@ cudaError_t side_for_current_device(Side **out) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     Side &sd = g_side[dev];
-    if (!sd.stream) {
-        if ((e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if (!sd.stream) {  // all three, or none (a failed creation is retried by the next call)
+        Side n;
+        if ((e = cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking)) == cudaSuccess &&
+            (e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming)) == cudaSuccess &&
+            (e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming)) == cudaSuccess) {
+            sd = n;
+        } else {
+            if (n.fork) cudaEventDestroy(n.fork);
+            if (n.stream) cudaStreamDestroy(n.stream);
+            return e;
+        }
     }
     *out = &sd;
     return cudaSuccess;
