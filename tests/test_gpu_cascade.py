@@ -159,3 +159,12 @@ def test_cascade_decode_pagefirst_pool():
                                                     head_dim=128, batch=12, prefix_len=400,
                                                     suffix_lo=0, suffix_hi=150, seed=71)
     run_cascade(case, 400, pagefirst=True)
+
+
+def test_cascade_decode_large_batch():
+    """1024 requests sharing a 600-token prefix, GQA 4: many prefix query
+    blocks per KV head and many suffix streams."""
+    case = workloads.make_shared_prefix_decode_case("cascade-b1024", num_q_heads=16, num_kv_heads=4,
+                                                    head_dim=128, batch=1024, prefix_len=600,
+                                                    suffix_lo=0, suffix_hi=120, seed=1024)
+    run_cascade(case, 600)

@@ -313,3 +313,28 @@ def test_cascade_extend_matches_oracle(Hq, Hkv, d, P):
         ref = orc.extend(q.cpu(), hk, hv, b.page_table, b.cached_lens, b.extend_lens, case.sm_scale)
         gu.check_attn(o, ref, f"{case.name} batch {bi}")
     assert mk.minisgl_debug_timeout_count() == 0
+
+
+def test_extend_maximum_batch():
+    """4096 requests (the largest batch the call takes; the per-request item
+    prefix fills 16 KB of shared memory) of 0-40 cached and 1-3 new tokens,
+    group size 4, against the oracle on every token."""
+    g = torch.Generator().manual_seed(4096)
+    B = 4096
+    cached = torch.randint(0, 41, (B,), generator=g).tolist()
+    ext = torch.randint(1, 4, (B,), generator=g).tolist()
+    case = _manual_case(cached, ext, Hq=16, Hkv=4, seed=4097)
+    b = case.batches[0]
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    hk, hv = gu.u16(pool_t[0, 0]), gu.u16(pool_t[1, 0])
+    k, v, q = per_batch[0]
+    pool = mk.KVPool(pool_t)
+    mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+    o = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), b.cached_lens.to(DEV),
+                               b.extend_lens.to(DEV), b.q_offsets.to(DEV), case.sm_scale)
+    torch.cuda.synchronize()
+    oracle.get().store_kv(hk, hv, k.cpu(), v.cpu(), b.out_loc)
+    ref = gu.parallel_oracle_extend(hk, hv, q, b.page_table, b.cached_lens, b.extend_lens, b.q_offsets,
+                                    case.sm_scale)
+    gu.check_attn(o, ref, "extend, 4096 requests")
+    assert mk.minisgl_debug_timeout_count() == 0
