@@ -280,6 +280,19 @@ def cpu_cores_used() -> int:
     return 1  # the oracle is single-threaded C
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
 def oracle_all_cores(case, pool_t, k_new, v_new, q, budget_s=10.0):
     """The same oracle on every host core: the batch's requests are dealt
     round-robin to one thread per core, each thread calling the oracle on its
@@ -893,7 +906,8 @@ def run_gpu(args, world, rank, local):
                 break
         dt = time.perf_counter() - t0
         cpu = {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
-               "kind": "oracle",
+               "kind": "oracle", "cpu_model": cpu_model(),
+               "host_cores_available": len(os.sched_getaffinity(0)),
                "sample": f"store_kv + decode of requests {reqs} (of {case.num_real} real) on layers "
                          f"{lay} (every layer has the same lengths, so the rate holds for all {L}), "
                          f"repeated {n}x, {dt:.1f} s, single-threaded fp64 C"}
@@ -989,7 +1003,7 @@ def run_reference(args, world, rank):
                    "real_requests": case.num_real, "sample_requests": reqs,
                    "parallelism": "single CPU thread"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores_used(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
