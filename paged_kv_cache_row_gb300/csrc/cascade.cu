@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(CascadeArgs a) {
     for (int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < nvec;
          v += ((int64_t)gridDim.x * blockDim.x) >> 5) {
         const int r = (int)(v / a.num_q_heads), h = (int)(v - (int64_t)r * a.num_q_heads);
-        // round 1
+        // first loads: nothing here depends on the split count
         const int seq = __ldg(a.seq_lens + r);
         const int cnt = sd.split_count[(int64_t)r * sd.num_kv_heads + h / G];  // stale if no suffix: unused then
         const float lp = lane < a.chunks ? a.pre_lse[(int64_t)lane * nvec + v] : -INFINITY;
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(CascadeArgs a) {
 #pragma unroll
                 for (int c = 0; c < PER; ++c) xp[k][c] = 0.f;
         }
-        // round 2
+        // second loads: the suffix splits
         const int n_suf = min(max(seq - a.shared_len, 0), sd.pt_width);
         const int S = n_suf > 0 ? min(min(cnt, sd.max_splits), SMAX) : 0;
         const int64_t sbase = v * sd.max_splits;
