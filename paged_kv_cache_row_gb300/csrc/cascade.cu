@@ -36,8 +36,8 @@ namespace {
 
 // one warp per (request, query head): merge the prefix chunks' fp32 partials
 // (lane c holds chunk c's LSE) and the suffix's split partials (lane s holds
-// split s's LSE; none when the request has no private positions).  Two
-// rounds of loads: first the context length, the split count and everything
+// split s's LSE; none when the request has no private positions).  Loads come
+// in two batches: first the context length, the split count and everything
 // of the prefix (LSEs and up to PF rows), which do not depend on the split
 // count; then the suffix LSEs and rows (at most SMAX).
 template <int D>
