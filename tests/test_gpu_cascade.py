@@ -168,3 +168,15 @@ def test_cascade_decode_large_batch():
                                                     head_dim=128, batch=1024, prefix_len=600,
                                                     suffix_lo=0, suffix_hi=120, seed=1024)
     run_cascade(case, 600)
+
+
+def test_cascade_decode_whole_table_shared():
+    """shared_len equal to the page-table width and every request reading
+    exactly the shared prefix: the suffix part has no columns at all."""
+    case = workloads.make_shared_prefix_decode_case("cascade-all-shared", num_q_heads=16, num_kv_heads=8,
+                                                    head_dim=128, batch=10, prefix_len=256,
+                                                    suffix_lo=0, suffix_hi=0, seed=6)
+    P = 256
+    case.page_table = case.page_table[:, :P].contiguous()  # width 256, a multiple of 32
+    seq = torch.full((case.batch,), P, dtype=torch.int32)
+    run_cascade(case, P, seq_override=seq)
