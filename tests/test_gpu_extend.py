@@ -338,3 +338,44 @@ def test_extend_maximum_batch():
                                     case.sm_scale)
     gu.check_attn(o, ref, "extend, 4096 requests")
     assert mk.minisgl_debug_timeout_count() == 0
+
+
+def test_page_table_row_stride_wider_than_width():
+    """Page tables that are a column slice of a wider buffer (row stride
+    larger than the width the call reads), for extend, decode and cascade
+    decode: the same results as with the compact table, bit for bit."""
+    case = _manual_case([100, 0, 333], [60, 200, 45], Hq=8, Hkv=2, seed=88)
+    b = case.batches[0]
+    pool_t, per_batch = workloads.make_extend_values(case, DEV)
+    k, v, q = per_batch[0]
+    pool = mk.KVPool(pool_t)
+    mk.minisgl_store_kv(pool, 0, k, v, b.out_loc.to(DEV))
+    W = b.page_table.shape[1]
+    wide = torch.full((b.page_table.shape[0], W + 96), -7, dtype=torch.int32)
+    wide[:, 16:16 + W] = b.page_table
+    pt_view = wide.to(DEV)[:, 16:16 + W]  # stride W + 96, width W
+    assert pt_view.stride(0) == W + 96 and pt_view.stride(1) == 1
+    args = [t.to(DEV) for t in (b.cached_lens, b.extend_lens, b.q_offsets)]
+    o1 = mk.minisgl_extend_attn(pool, 0, q, b.page_table.to(DEV), *args, case.sm_scale)
+    o2 = mk.minisgl_extend_attn(pool, 0, q, pt_view, *args, case.sm_scale)
+    seq = (b.cached_lens + b.extend_lens).to(DEV)
+    qd = q[(b.q_offsets[1:] - 1).long().to(DEV)].contiguous()
+    d1 = mk.minisgl_decode_attn(pool, 0, qd, b.page_table.to(DEV), seq, case.sm_scale)
+    d2 = mk.minisgl_decode_attn(pool, 0, qd, pt_view, seq, case.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(d1, d2)
+    sc = workloads.make_shared_prefix_decode_case("stride-cascade", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                                                  batch=7, prefix_len=300, suffix_lo=1, suffix_hi=90, seed=89)
+    spool_t, sk, sv, sq = workloads.make_decode_values(sc, DEV)
+    spool = mk.KVPool(spool_t)
+    mk.minisgl_store_kv(spool, 0, sk[0], sv[0], sc.out_loc.to(DEV))
+    SW = sc.page_table.shape[1]
+    swide = torch.full((sc.batch, SW + 64), -7, dtype=torch.int32)
+    swide[:, :SW] = sc.page_table
+    sview = swide.to(DEV)[:, :SW]
+    c1 = mk.minisgl_cascade_decode_attn(spool, 0, sq[0], sc.page_table.to(DEV), sc.seq_lens.to(DEV), 300,
+                                        sc.sm_scale)
+    c2 = mk.minisgl_cascade_decode_attn(spool, 0, sq[0], sview, sc.seq_lens.to(DEV), 300, sc.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+    assert mk.minisgl_debug_timeout_count() == 0
