@@ -28,6 +28,10 @@
 //   * A warp whose segment covers a whole stream writes the bf16 output; a
 //     stream cut across segments leaves normalised fp32 partials and their
 //     natural-log LSE in the workspace, and decode_merge_kernel combines them.
+//   * For the shared-prefix (cascade) call: a length offset (a request's row
+//     starts past the shared positions), fp32 partials for whole streams too
+//     with no merge launch (the cascade merge combines them with the prefix
+//     part), and a grid limited to the SMs the prefix part leaves free.
 #include <cfloat>
 #include <mutex>
 

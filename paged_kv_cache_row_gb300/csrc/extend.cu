@@ -21,8 +21,9 @@
 //     with 16-byte cp.async into the 128-byte-swizzled layout the tensor core
 //     reads (K as a K-major B operand, V as an MN-major B operand), two
 //     stages deep; completion is tracked by mbarriers (cp.async.mbarrier.arrive).
-//     A lane copies 4 chunks of each of its rows, so the address work per
-//     copy is small: these warps share schedulers with softmax warps.
+//     A lane copies d/32 chunks (4 at d 128) of each of its rows, so the
+//     address work per copy is small: these warps share schedulers with
+//     softmax warps.
 //   * Warp 11 (one lane) issues tcgen05.mma.  Per query tile X: S_X = Q_X K^T
 //     (M = N = 128) into tensor memory; O_X += P_X V with P_X read from
 //     tensor memory.  The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
@@ -48,7 +49,14 @@
 //     O_B from 384 (d columns each).  Shared memory: Q_A, Q_B (128 rows of
 //     2d bytes each), two K/V stages (two such tiles each): 192 KB at d 128.
 //   * The work-ticket counter of the dynamic schedule is the caller's when
-//     given, else one of 64 library slots taken in turn.
+//     given, else one of 64 library slots taken in turn.  A stream's query
+//     blocks are handed out last block first (the causal limit makes it the
+//     longest), so the items drawn at the end of a launch are short ones.
+//   * Modes for the shared-prefix calls: prefix-only (every new token sees
+//     exactly its C cached positions; fp32 rows and LSEs out), with the
+//     prefix-chunk geometry computed instead of read; len_offset (a request's
+//     page-table row starts past the shared positions); and a fold of an
+//     fp32 partial over other positions into the bf16 output by log-sum-exp.
 //   * Every mbarrier wait is bounded in time; a wait that runs out sets a
 //     flag, the kernel finishes without further waiting (its output is then
 //     garbage) and a device counter of such events is increased.
