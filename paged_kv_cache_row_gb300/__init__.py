@@ -130,6 +130,20 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _rows_ok(t: torch.Tensor, n: int, row: int) -> bool:
+    """True when t is [n, ...] and each t[i] is `row` contiguous elements
+    (read from the shape and strides alone: indexing a tensor costs several
+    microseconds of host time per call)."""
+    if t.dim() < 2 or t.shape[0] != n:
+        return False
+    expect = 1
+    for size, stride in zip(reversed(t.shape[1:]), reversed(t.stride()[1:])):
+        if size != 1 and stride != expect:
+            return False
+        expect *= size
+    return expect == row
+
+
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
     if not t.is_cuda:
         raise MinisglError(f"{name} must be a CUDA tensor")
@@ -183,7 +197,7 @@ def minisgl_store_kv(pool: KVPool, layer: int, k: torch.Tensor, v: torch.Tensor,
     n = out_loc.numel()
     row = pool.num_kv_heads * pool.head_dim
     for t, nm in ((k, "k"), (v, "v")):
-        if t.shape[0] != n or t[0].numel() != row or not t[0].is_contiguous():
+        if not _rows_ok(t, n, row):
             raise MinisglError(f"{nm} must be [n_tokens, H_kv, d] with contiguous rows")
     if not out_loc.is_contiguous():
         raise MinisglError("out_loc must be contiguous")
@@ -452,7 +466,7 @@ def minisgl_store_decode_attn(pool: KVPool, layer: int, k: torch.Tensor, v: torc
         raise MinisglError("q must be contiguous [B, H_q, head_dim]")
     row = pool.num_kv_heads * d
     for t, nm in ((k, "k"), (v, "v")):
-        if t.shape[0] != B or t[0].numel() != row or not t[0].is_contiguous():
+        if not _rows_ok(t, B, row):
             raise MinisglError(f"{nm} must be [B, H_kv, d] with contiguous rows")
     if page_table.dim() != 2 or page_table.shape[0] != B or page_table.stride(1) != 1:
         raise MinisglError("page_table must be [B, W] with unit column stride")
