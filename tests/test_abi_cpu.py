@@ -160,3 +160,29 @@ def test_kv_pool_bytes_golden():
     got = p.kv_pool_bytes(fx["num_layers"], fx["num_kv_heads"], fx["head_dim"], fx["num_tokens"],
                           fx["elem_bytes"])
     assert got == fx["expected_bytes"]
+
+
+def test_binding_row_check_reads_shapes_and_strides():
+    """The binding's check that k / v hold [n, ...] rows of `row` contiguous
+    elements agrees with indexing a row and asking torch, on layouts that pass
+    and layouts that do not (and accepts zero rows, which indexing cannot)."""
+    import torch
+    from paged_kv_cache_row_gb300 import _rows_ok
+
+    def by_indexing(t, n, row):
+        return t.shape[0] == n and t[0].numel() == row and t[0].is_contiguous()
+
+    cases = [torch.zeros(5, 8, 128),                       # dense
+             torch.zeros(5, 2048)[:, :1024],               # rows padded to a wider stride
+             torch.zeros(5, 8, 256)[:, :, :128],           # heads padded: rows not contiguous
+             torch.zeros(8, 5, 128).transpose(0, 1),       # token and head axes swapped
+             torch.zeros(5, 1, 1024),                      # a size-1 axis with any stride
+             torch.zeros(5, 128, 8).transpose(1, 2),       # channels strided
+             torch.zeros(10, 8, 128)[::2],                 # every other token
+             torch.zeros(5, 8, 128, 1),                    # trailing size-1 axis
+             torch.zeros(5, 4, 128)]                       # wrong row length
+    for t in cases:
+        assert _rows_ok(t, 5, 1024) == by_indexing(t, 5, 1024), (tuple(t.shape), t.stride())
+        assert not _rows_ok(t, 6, 1024)
+    assert _rows_ok(torch.zeros(0, 8, 128), 0, 1024)
+    assert not _rows_ok(torch.zeros(1024), 1024, 1)
