@@ -877,12 +877,21 @@ def run_gpu(args, world, rank, local):
     # Copies run on their own streams so they overlap the layers: the page
     # table, seq_lens and out_loc go first, then each layer's k, v and q, and
     # each layer's output comes back as soon as that layer is done.  The
-    # compute stream waits for the last copy, so the timed region holds all of
-    # them.
+    # compute stream waits for the inputs only before layers 0, 1, 2, 4, 8,
+    # 16, ..., each time for those of the layers up to about twice as far
+    # (an event wait between two calls ends the programmatic launch overlap
+    # of the second with the first, and the copies run far ahead of the
+    # layers).  The compute stream waits for the last output copy, so the
+    # timed region holds all of them.
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     meta_ev = torch.cuda.Event()
     in_ev = [torch.cuda.Event() for _ in range(L)]
     out_ev = [torch.cuda.Event() for _ in range(L)]
+    in_wait = {0: 0}
+    w = 1
+    while w < L:
+        in_wait[w] = min(L - 1, 2 * w + 1)  # before layer w: the inputs of layers <= 2w + 1
+        w *= 2
 
     def e2e_step():
         h2d.wait_stream(stream)  # the previous step is done with the device inputs
@@ -896,7 +905,8 @@ def run_gpu(args, world, rank, local):
                 in_ev[l].record(h2d)
         stream.wait_event(meta_ev)
         for l in range(L):
-            stream.wait_event(in_ev[l])
+            if l in in_wait:
+                stream.wait_event(in_ev[in_wait[l]])
             mk.minisgl_store_decode_attn(pool, l, d_in[0][l], d_in[1][l], d_in[5], d_in[2][l], d_in[3],
                                          d_in[4], case.sm_scale, out=outs[l], workspace=ws)
             out_ev[l].record(stream)
