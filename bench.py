@@ -359,6 +359,18 @@ def graph_ms(fn, n, replays, stream):
     return ms
 
 
+def input_wait_schedule(L: int) -> dict:
+    """Layers before which the e2e step's compute stream waits for input
+    copies: {layer: last layer whose inputs the wait covers}, at layers 0, 1,
+    2, 4, 8, ... (each wait covers the inputs of the layers up to about twice
+    as far), so every layer's inputs are covered by the time it runs."""
+    sched, w = {0: 0}, 1
+    while w < L:
+        sched[w] = min(L - 1, 2 * w + 1)
+        w *= 2
+    return sched
+
+
 def headline_case(layers: int):
     """The Llama-3-8B decode workload with its pool at 1.2x the live tokens,
     or 1.05x when the device has too little free memory for that (the pool of
@@ -887,11 +899,7 @@ def run_gpu(args, world, rank, local):
     meta_ev = torch.cuda.Event()
     in_ev = [torch.cuda.Event() for _ in range(L)]
     out_ev = [torch.cuda.Event() for _ in range(L)]
-    in_wait = {0: 0}
-    w = 1
-    while w < L:
-        in_wait[w] = min(L - 1, 2 * w + 1)  # before layer w: the inputs of layers <= 2w + 1
-        w *= 2
+    in_wait = input_wait_schedule(L)
 
     def e2e_step():
         h2d.wait_stream(stream)  # the previous step is done with the device inputs

@@ -112,3 +112,18 @@ def test_committed_profiles_name_their_sources():
         text = open(os.path.join(prof, name)).read()
         if "traffic_bytes_per_launch" in text:
             assert "kernel_source_sha256_16" in text, name
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 5, 28, 32, 33, 64])
+def test_e2e_input_waits_cover_every_layer(L):
+    """Before each layer runs, some earlier (or its own) wait covers its inputs,
+    and no wait points past the last layer."""
+    sched = bench.input_wait_schedule(L)
+    assert 0 in sched and sched[0] >= 0
+    covered = -1
+    for layer in range(L):
+        if layer in sched:
+            assert layer <= sched[layer] <= L - 1
+            covered = max(covered, sched[layer])
+        assert covered >= layer, (L, layer)
+    assert len(sched) <= L.bit_length() + 1
